@@ -1,0 +1,277 @@
+/*
+ * zerostep.h — C ABI of the partitioned mixed-precision ZeRO Adam step on one
+ * GB300 GPU (sm_103a).
+ *
+ * The operation (the data-parallel hot path of ZeRO stages 1-3):
+ *   N_d data-parallel ranks each hold a half-precision (fp16 or bf16)
+ *   gradient of the whole flat parameter vector.  Rank r owns a 1/N_d
+ *   partition of that vector.  One step
+ *     (a2) reduce-scatters the gradients: rank r's fp32 gradient is the
+ *          element-wise sum over all ranks of their gradients on r's
+ *          partition;
+ *     (a3) multiplies it by 1/S (S = the loss scale, a power of two);
+ *     (a4) skips the whole step if any element of any partition is NaN/Inf,
+ *          leaving every buffer bit-for-bit unchanged (only a dynamic loss
+ *          scale is lowered);
+ *     (a5) optionally scales the gradient by min(1, max_norm / (||g||_2 + 1e-6)),
+ *          the norm taken over all partitions;
+ *     (a6) applies Adam or AdamW to the partition's fp32 master weights,
+ *          momentum and variance;
+ *     (a7) rounds the new master weights to half precision (nearest, ties to
+ *          even) and writes them at the partition's place in the flat
+ *          half-precision parameter buffer, i.e. the layout an all-gather of
+ *          all partitions produces;
+ *     (a8) commits the step (t <- t + 1) or records the skip.
+ *   Sources — five web pages on DeepSpeed ZeRO:
+ *     "DeepSpeed ZeRO" (formulaic.cloudchewie.com): "ZeRO Stage 1: 切分优化器状态"
+ *       ("权重更新的触发条件": skip on NaN/Inf and in-place fp32 -> fp16 copy;
+ *       "以 AdaW 为例": the m, v, W update; "具体训练步骤": local update of the
+ *       1/N_d slice, cast, all-gather), "ZeRO Stage 2: 切分梯度" (reduce-scatter;
+ *       fp32 gradient slice made from the reduce-scattered half gradient;
+ *       per-element independence of the update), "ZeRO Stage 3: 切分参数"
+ *       ("参数的初始化和切割": flatten, pad, [start, end) per rank), "相关分析"
+ *       ("Constant Size Buffer": fixed-size buckets), "配置说明" (loss scale);
+ *     "zero-optimizer" (codezrq.github.io), 2.5 ReduceScatter and 2.6 AllGather;
+ *       "一. 优化前" (gradient-norm computation in fused buffers);
+ *     "ZeRO 技术原理：基础与实现" (jianzhnie.github.io), 3.1.1 ZeRO-1 and
+ *       3.3.1 "初始化——模型参数的分割" (per-rank [start, end) of a flat tensor);
+ *     "千亿参数模型如何塞进有限显卡：ZeRO如何用分片消除数据并行的内存冗余"
+ *       (answer.freetools.me), "Stage 2：梯度分片" (Reduce-Scatter to the owner).
+ *   Where the pages are silent the library takes these readings: the reduction
+ *   is a sum in fp32, in ascending rank order from +0, with no rounding to
+ *   half in between; Adam is bias-corrected (Kingma and Ba) unless
+ *   bias_correction = 0; AdamW decay is decoupled, W <- W (1 - lr wd), applied
+ *   before the update; the overflow test is on the reduced unscaled gradient.
+ *
+ * Simulation on one GPU: the N_d ranks' gradient buffers all live in this
+ * GPU's memory.  A call either processes every rank's partition at once
+ * (rank = -1) or one rank's partition (rank = r).
+ *
+ * Conventions for every entry point:
+ *  - The caller allocates and owns every buffer; the library allocates no
+ *    memory and keeps no state between calls other than read-only device
+ *    properties.  Pointers named *_dev or documented as device pointers must
+ *    be CUDA device pointers of the current device; all others are host
+ *    pointers read during the call only.
+ *  - Device work is enqueued on `stream` (NULL = the legacy default stream)
+ *    and runs asynchronously; nothing synchronises the host.  Calls that use
+ *    the same workspace or state must be ordered on one stream.
+ *  - Arguments are validated on the host before anything is enqueued; on an
+ *    error nothing is enqueued.  Return values: ZERO_OK (0) or a negative
+ *    code below.  A value <= ZERO_ECUDA_BASE is ZERO_ECUDA_BASE - cudaError_t
+ *    of a failed launch.  Kernels never trap: numerical overflow is reported
+ *    through zero_step_state, not as an error.
+ *  - Vector buffers must be 16-byte aligned (ZERO_EALIGN otherwise).
+ */
+#ifndef ZEROSTEP_H
+#define ZEROSTEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *zero_stream_t; /* the same type as cudaStream_t */
+
+enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = -1,        /* null pointer, bad size, world, rank, dtype, config or layout */
+    ZERO_EALIGN = -2,        /* a buffer is not 16-byte aligned */
+    ZERO_ESPACE = -3,        /* workspace smaller than zero_workspace_bytes() */
+    ZERO_ECUDA_BASE = -1000  /* ZERO_ECUDA_BASE - cudaError_t */
+};
+
+#define ZERO_MAX_WORLD 1024
+
+typedef enum { ZERO_F16 = 0, ZERO_BF16 = 1 } zero_dtype;
+
+/*
+ * Partition layout of the flat parameter vector (step a1).
+ * Tensor k starts at offset_k = round_up(offset_{k-1} + numel_{k-1}, align).
+ * Not bucketed (bucket_numel = 0): the vector is padded to a multiple of
+ * world * align and rank r owns [r * owned, (r + 1) * owned).
+ * Bucketed: the vector is cut into buckets of bucket_numel elements (the last
+ * one padded to a multiple of world * align); rank r owns slice r of every
+ * bucket, so its elements are, in order, bucket 0 slice r, bucket 1 slice r, ...
+ * Padding elements must be zero in every gradient, master and moment buffer
+ * (they then stay zero).
+ */
+typedef struct {
+    int64_t numel;            /* sum of tensor sizes (unpadded) */
+    int64_t flat_numel;       /* end of the last tensor, alignment gaps included */
+    int64_t padded_numel;     /* length of the padded flat vector */
+    int64_t owned_numel;      /* elements each rank owns */
+    int64_t bucket_numel;     /* 0: one contiguous partition per rank */
+    int64_t num_buckets;      /* 1 when not bucketed (0 for an empty vector) */
+    int64_t slice_numel;      /* a rank's slice of a full bucket (= owned_numel if not bucketed) */
+    int64_t last_slice_numel; /* a rank's slice of the last bucket (= owned_numel if not bucketed) */
+    int32_t world;            /* N_d, 1 .. ZERO_MAX_WORLD */
+    int32_t align_elems;      /* tensor alignment in elements, a multiple of 8 */
+} zero_layout;
+
+/* Optimizer configuration.  Field names follow DeepSpeed's JSON config
+ * ("DeepSpeed ZeRO", "配置说明": lr, betas, eps, weight_decay; fp16.loss_scale
+ * = 0 selects the dynamic loss scale). */
+typedef struct {
+    double lr;
+    double beta1, beta2;
+    double eps;
+    double weight_decay;
+    int32_t adamw;           /* 1: decoupled decay (AdamW); 0: coupled L2 term added to g */
+    int32_t bias_correction; /* 1: Kingma-Ba bias correction; 0: the pages' formula as printed */
+    double max_grad_norm;    /* > 0: clip by the global L2 norm (two passes); 0: no clipping */
+    int32_t dynamic_scale;   /* 1: S <- max(S * backoff, min_scale) on overflow and
+                                S <- S * growth after growth_interval good steps in a row */
+    int32_t growth_interval;
+    double backoff, growth, min_scale;
+} zero_adam_cfg;
+
+/*
+ * Step state, DEVICE-resident (64 bytes, 8-byte aligned), owned by the
+ * caller.  Initialise a host copy with zero_state_init and copy it to the
+ * device.  The kernels read it at the start of a step and zero_step_finalize
+ * (or zero_step_fused) updates it at the end.
+ */
+typedef struct {
+    int64_t t;          /* committed (not skipped) steps */
+    double beta1_pow;   /* beta1^t as a running product in binary64 */
+    double beta2_pow;   /* beta2^t as a running product in binary64 */
+    double sumsq;       /* global sum of squares of the unscaled gradient (last clip step) */
+    float loss_scale;   /* S, a power of two */
+    float clip_coef;    /* clip coefficient of the last clipped step */
+    int32_t good_steps; /* good steps since the last overflow or growth */
+    int32_t overflow;   /* 1 if the last step was skipped */
+    int32_t found_inf;  /* OR of the non-finite flags of the step in progress */
+    int32_t cur;        /* ping-pong slot (0/1) holding the current master/m/v/params */
+    int32_t skipped;    /* number of skipped steps */
+    int32_t reserved;
+} zero_step_state;
+
+/* Human-readable text for a return code (static storage). */
+const char *zero_strerror(int code);
+
+/* ABI version: 1. */
+int zero_version(void);
+
+/*
+ * Step (a1): the partition layout.  Host-only, pure.
+ *  numel[n_tensors]: tensor sizes (>= 0).  world: N_d in 1 .. ZERO_MAX_WORLD.
+ *  align_elems: tensor alignment in elements, a positive multiple of 8
+ *  (64 gives 128-byte aligned fp16/bf16 tensors).  bucket_numel: 0 or a
+ *  positive multiple of world * 8.  tensor_offset_out[n_tensors] (may be NULL)
+ *  receives each tensor's flat offset.
+ * Pages: "DeepSpeed ZeRO", "ZeRO Stage 3", "参数的初始化和切割" (flatten, pad so
+ * the length divides by the data-parallel size, [start, end) per rank);
+ * "ZeRO 技术原理", 3.3.1 (partition_size per rank, start = partition_size *
+ * rank; the floor division there is read as padding so no element is lost);
+ * "DeepSpeed ZeRO", "Constant Size Buffer" (buckets).
+ */
+int zero_partition_layout(int n_tensors, const int64_t *numel, int world, int align_elems,
+                          int64_t bucket_numel, int64_t *tensor_offset_out, zero_layout *out);
+
+/* Fill *host_state with the state before the first step: t = 0, beta powers
+ * 1, loss_scale (a positive power of two), clip_coef 1, everything else 0. */
+int zero_state_init(zero_step_state *host_state, float loss_scale);
+
+/* Bytes of workspace the device-side reductions need for a group of `world`
+ * ranks (a few tens of KB).  Its contents need no initialisation. */
+size_t zero_workspace_bytes(int world);
+
+/*
+ * Step (a2): reduce-scatter sum, g[j] = sum over q = 0 .. world-1 of
+ * float(grads[q][.]) in ascending q, fp32, not unscaled.
+ *  grads: HOST array of `world` DEVICE pointers, one gradient buffer per rank.
+ *  grads_are_slices: 0 = each buffer is the full padded flat vector;
+ *    1 = each buffer holds only the elements `rank` owns, in order (needs rank >= 0).
+ *  rank = -1: every partition; g_out (device, padded_numel floats) is in flat
+ *    order.  rank = r: r's partition; g_out (owned_numel floats) in r's order.
+ * Pages: "zero-optimizer", 2.5 ReduceScatter; "DeepSpeed ZeRO", ZeRO Stage 2.
+ */
+int zero_reduce_scatter_sum(const void *const *grads, int grads_are_slices, zero_dtype dtype,
+                            const zero_layout *layout, int rank, float *g_out,
+                            zero_stream_t stream);
+
+/*
+ * Step (a4): *flag_dev |= 1 if any g[j] * inv_scale (j < n) is NaN or +-Inf;
+ * otherwise *flag_dev is left as it is (clear it before the first call; pass
+ * &state->found_inf to feed zero_adam_step).  g: device, n floats.
+ * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "权重更新的触发条件".
+ */
+int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *flag_dev,
+                        zero_stream_t stream);
+
+/*
+ * Step (a5): *sumsq_dev = sum over j < n of (g[j] * inv_scale)^2, accumulated
+ * beyond binary64 accuracy (exact squares, compensated sums) in an order fixed
+ * by n and the device, so repeated calls give the same bits.  g: device;
+ * sumsq_dev: device double; ws: device workspace of ws_bytes >=
+ * zero_workspace_bytes(1).
+ * Pages: "zero-optimizer", "一. 优化前" (gradient-norm computation over fused
+ * buffers); the clip rule itself is a reading (see zero_adam_cfg).
+ */
+int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
+                   size_t ws_bytes, zero_stream_t stream);
+
+/*
+ * Steps (a3), (a5 clip), (a6), (a7) on n elements in place, for the reduced
+ * gradient g that zero_reduce_scatter_sum produced (not yet unscaled).
+ * Reads from state_dev: loss_scale, t and the beta powers (the update is step
+ * t + 1), found_inf (if set the call changes nothing) and, when
+ * cfg->max_grad_norm > 0, sumsq (from zero_grad_norm) for the clip.
+ * master, m, v: device fp32 (n); half_out: device fp16/bf16 (n) receiving
+ * round-to-nearest-even of the new master weights.  Call zero_step_finalize
+ * afterwards to commit the step.
+ * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "以 AdaW 为例" and "权重更新的触发条件".
+ */
+int zero_adam_step(const float *g, float *master, float *m, float *v, void *half_out,
+                   zero_dtype dtype, int64_t n, const zero_adam_cfg *cfg,
+                   const zero_step_state *state_dev, zero_stream_t stream);
+
+/*
+ * Step (a8): end a step.  If state_dev->found_inf: overflow = 1, skipped += 1,
+ * and with a dynamic scale S <- max(S * backoff, min_scale), good_steps = 0.
+ * Otherwise: overflow = 0, t += 1, beta powers advance, good_steps += 1 (and
+ * S <- S * growth after growth_interval of them), and if flip_slot the
+ * ping-pong slot cur is toggled.  found_inf is cleared either way.
+ * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "权重更新的触发条件"; "配置说明".
+ */
+int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int flip_slot,
+                       zero_stream_t stream);
+
+/*
+ * The whole step (a2)-(a8), fused.
+ *  grads, grads_are_slices, dtype, layout, rank: as zero_reduce_scatter_sum.
+ *  master[2], m[2], v[2]: HOST arrays of two DEVICE pointers each (ping-pong
+ *    slots) to fp32 buffers of padded_numel (rank = -1, flat order) or
+ *    owned_numel (rank = r, r's order) elements.
+ *  params[2]: HOST array of two DEVICE pointers to the flat half-precision
+ *    parameter buffer (padded_numel elements, all-gather layout); the step
+ *    writes the elements of the partitions it processes.
+ *  The step reads slot state->cur and writes slot 1 - cur, then toggles cur
+ *  when the step commits; a skipped step writes only the unused slot, so the
+ *  current slot stays bit-for-bit unchanged.
+ *  Without clipping (cfg->max_grad_norm == 0) the step is ONE pass over the
+ *  data: the slots must be distinct buffers.  With clipping it is two passes
+ *  (norm, then update); the two slots may then be the same buffer (in place).
+ *  g_stage: NULL, or (clip only) a device fp32 buffer with the length of
+ *    master that keeps the reduced gradient between the passes instead of
+ *    reducing it twice (2 * N_d bytes read per element are replaced by 8).
+ *  state_dev: device step state.  ws: device workspace of ws_bytes >=
+ *    zero_workspace_bytes(layout->world).
+ * Pages: all of the above; the ping-pong slots are this library's way to
+ * skip a step bit-exactly without a second pass over the gradients.
+ */
+int zero_step_fused(const void *const *grads, int grads_are_slices, zero_dtype dtype,
+                    const zero_layout *layout, int rank, float *const master[2],
+                    float *const m[2], float *const v[2], void *const params[2], float *g_stage,
+                    const zero_adam_cfg *cfg, zero_step_state *state_dev, void *ws,
+                    size_t ws_bytes, zero_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZEROSTEP_H */

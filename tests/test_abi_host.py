@@ -1,0 +1,166 @@
+"""The C-ABI library on the host, without a GPU: it loads, exports every
+symbol include/zerostep.h declares, its structs match the header, its
+partition layout (a host-only function) equals the oracle's independent
+layout bit for bit, and invalid arguments are rejected before any device
+work is enqueued."""
+import ctypes
+import os
+import random
+import re
+import subprocess
+
+import pytest
+
+import oracle
+from synth.workloads import ALL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zerostep.h")
+
+
+@pytest.fixture(scope="module")
+def zs():
+    from zero_partitioned_mixed_step_gb300 import _build
+    _build.build()
+    import zero_partitioned_mixed_step_gb300 as zs
+    zs._abi.lib()
+    return zs
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(zero_\w+)\s*\(", text,
+                                 re.M)))
+
+
+def test_exports_every_declared_symbol(zs):
+    names = declared_functions()
+    assert len(names) == 11, names
+    so = ctypes.CDLL(zs._build.LIB)
+    for n in names:
+        assert hasattr(so, n), n
+    assert set(names) == set(zs._abi.SIGNATURES)
+
+
+def test_structs_match_header(tmp_path, zs):
+    src = tmp_path / "off.c"
+    fields = {"zero_layout": zs.Layout, "zero_adam_cfg": zs.AdamCfg,
+              "zero_step_state": zs.StepState}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "zerostep.h"', "int main(void){"]
+    for cname, cls in fields.items():
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0;}")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "off"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = dict(line.rsplit(" ", 1) for line in subprocess.run(
+        [str(exe)], capture_output=True, text=True, check=True).stdout.split("\n") if line)
+    for cname, cls in fields.items():
+        assert int(out[cname]) == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert int(out[f"{cname}.{f}"]) == getattr(cls, f).offset, (cname, f)
+
+
+def _same(lay_c, offs_c, lay_o):
+    assert lay_c.numel == lay_o.numel
+    assert lay_c.flat_numel == lay_o.flat_end
+    assert lay_c.padded_numel == lay_o.padded
+    assert lay_c.owned_numel == lay_o.owned
+    assert lay_c.num_buckets == lay_o.num_buckets
+    if lay_o.bucket:
+        assert lay_c.slice_numel == lay_o.slice
+        assert lay_c.last_slice_numel == lay_o.last_slice
+    assert list(offs_c) == list(lay_o.offsets)
+
+
+@pytest.mark.parametrize("wl", ALL, ids=lambda w: w.name)
+def test_layout_matches_oracle_on_workloads(zs, wl):
+    lay_c, offs = zs.zero_partition_layout(wl.numels, wl.world, 64, wl.bucket)
+    _same(lay_c, offs, oracle.layout(wl.numels, wl.world, 64, wl.bucket))
+
+
+def test_layout_matches_oracle_random(zs):
+    rnd = random.Random(1)
+    for _ in range(400):
+        world = rnd.choice([1, 2, 3, 4, 7, 8, 16, 64, 100, 1024])
+        align = rnd.choice([8, 16, 64, 128])
+        numels = [rnd.choice([0, 1, 7, 8, 63, 64, 65, rnd.randint(0, 100000)])
+                  for _ in range(rnd.randint(0, 12))]
+        bucket = rnd.choice([0, 0, world * 8 * rnd.randint(1, 50)])
+        lay_c, offs = zs.zero_partition_layout(numels, world, align, bucket)
+        _same(lay_c, offs, oracle.layout(numels, world, align, bucket))
+
+
+def test_layout_rejects_bad_arguments(zs):
+    lib = zs._abi.lib()
+    out = zs.Layout()
+    arr = (ctypes.c_int64 * 2)(10, 20)
+    bad = [(2, arr, 0, 64, 0), (2, arr, 1025, 64, 0), (2, arr, 4, 12, 0), (2, arr, 4, 0, 0),
+           (2, arr, 4, 64, 100), (2, arr, 4, 64, -32), (-1, arr, 4, 64, 0), (2, None, 4, 64, 0)]
+    for n, a, w, al, b in bad:
+        assert lib.zero_partition_layout(n, a, w, al, b, None, ctypes.byref(out)) == zs._abi.EINVAL
+    neg = (ctypes.c_int64 * 1)(-5)
+    assert lib.zero_partition_layout(1, neg, 4, 64, 0, None, ctypes.byref(out)) == zs._abi.EINVAL
+
+
+def test_state_init_and_workspace(zs):
+    s = zs.zero_state_init(4096.0)
+    assert (s.t, s.beta1_pow, s.beta2_pow, s.loss_scale, s.clip_coef, s.cur, s.found_inf) == \
+        (0, 1.0, 1.0, 4096.0, 1.0, 0, 0)
+    lib = zs._abi.lib()
+    st = zs.StepState()
+    for bad in (0.0, -2.0, 3.0, float("inf"), float("nan")):
+        assert lib.zero_state_init(ctypes.byref(st), bad) == zs._abi.EINVAL
+    assert zs.zero_workspace_bytes(1) >= 256 + 8 * 4096
+    assert lib.zero_workspace_bytes(0) == 0 and lib.zero_workspace_bytes(1025) == 0
+    assert lib.zero_strerror(zs._abi.EALIGN).decode().startswith("buffer")
+
+
+def test_entry_points_validate_before_launch(zs):
+    """Invalid calls return an error code without touching the device (this
+    machine has none, so a launch would fail with a CUDA error instead)."""
+    lib = zs._abi.lib()
+    lay, _ = zs.zero_partition_layout([1000], 2)
+    cfg = zs.adam_cfg()
+    fake = 1 << 20  # never dereferenced: validation fails first
+    g2 = (ctypes.c_void_p * 2)(fake, fake)
+    slots = (ctypes.c_void_p * 2)(fake, fake + 4096)
+    same = (ctypes.c_void_p * 2)(fake, fake)
+    E = zs._abi
+    # rank out of range, dtype, slices without rank
+    assert lib.zero_reduce_scatter_sum(g2, 0, 0, ctypes.byref(lay), 2, fake, None) == E.EINVAL
+    assert lib.zero_reduce_scatter_sum(g2, 0, 7, ctypes.byref(lay), 0, fake, None) == E.EINVAL
+    assert lib.zero_reduce_scatter_sum(g2, 1, 0, ctypes.byref(lay), -1, fake, None) == E.EINVAL
+    # misaligned gradient pointer
+    g_mis = (ctypes.c_void_p * 2)(fake + 2, fake)
+    assert lib.zero_reduce_scatter_sum(g_mis, 0, 0, ctypes.byref(lay), 0, fake, None) == E.EALIGN
+    # one-pass step with aliased slots cannot skip bit-exactly
+    rc = lib.zero_step_fused(g2, 0, 0, ctypes.byref(lay), -1, same, slots, slots, slots, None,
+                             ctypes.byref(cfg), fake, fake, 1 << 20, None)
+    assert rc == E.EINVAL
+    # workspace too small
+    rc = lib.zero_step_fused(g2, 0, 0, ctypes.byref(lay), -1, slots, slots, slots, slots, None,
+                             ctypes.byref(cfg), fake, fake, 16, None)
+    assert rc == E.ESPACE
+    # a staging buffer without clipping
+    rc = lib.zero_step_fused(g2, 0, 0, ctypes.byref(lay), -1, slots, slots, slots, slots, fake,
+                             ctypes.byref(cfg), fake, fake, 1 << 20, None)
+    assert rc == E.EINVAL
+    # bad optimizer configuration
+    for kw in (dict(beta1=1.0), dict(eps=0.0), dict(lr=-1.0), dict(max_grad_norm=-1.0),
+               dict(dynamic_scale=True, backoff=0.3), dict(dynamic_scale=True, growth_interval=0)):
+        c = zs.adam_cfg(**kw)
+        rc = lib.zero_step_fused(g2, 0, 0, ctypes.byref(lay), -1, slots, slots, slots, slots,
+                                 None, ctypes.byref(c), fake, fake, 1 << 20, None)
+        assert rc == E.EINVAL, kw
+    # a layout whose fields do not agree
+    broken = zs.Layout.from_buffer_copy(bytes(lay))
+    broken.owned_numel += 8
+    assert lib.zero_reduce_scatter_sum(g2, 0, 0, ctypes.byref(broken), -1, fake, None) == E.EINVAL
+    assert lib.zero_check_overflow(fake + 4, 10, 1.0, fake, None) == E.EALIGN
+    assert lib.zero_grad_norm(fake, 10, 1.0, fake, fake, 8, None) == E.ESPACE
+    assert lib.zero_adam_step(fake, fake, fake, fake, fake, 0, -1, ctypes.byref(cfg), fake,
+                              None) == E.EINVAL

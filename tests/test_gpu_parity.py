@@ -1,0 +1,281 @@
+"""The CUDA step (through the C ABI) against the CPU oracle, element by
+element, on the same seeded inputs, step after step.
+
+Sizes are small enough for the oracle to finish in seconds but span many
+CTAs, several ranks and ragged tails; every workload's structure (tensor
+list, alignment, buckets, rank view, dtype, loss scaling, clipping,
+overflow injection) is exercised.  Full-size workloads are in
+test_gpu_fullsize.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.workloads import CFG1, CFG2, CFG3, CFG4, CFG5, decoder_8b_numels, gpt2_small_numels
+import zero_partitioned_mixed_step_gb300 as zs
+from zs_harness import (Lockstep, assert_close, gen_grads, half_bits, lib_cfg, oracle_cfg,
+                        rank_index, to_dev_half)
+
+pytestmark = pytest.mark.gpu
+
+
+def _small_gpt2():
+    d, vocab, ctx = 64, 1000, 128
+    t = [vocab * d, ctx * d]
+    for _ in range(2):
+        t += [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
+    return tuple(t + [d, d])
+
+
+def _small_decoder():
+    d, ffn, vocab, kv = 64, 224, 1000, 16
+    t = [vocab * d]
+    for _ in range(2):
+        t += [d, d * d, kv * d, kv * d, d * d, d, ffn * d, ffn * d, d * ffn]
+    return tuple(t + [d, vocab * d])
+
+
+SMALL = {
+    # the whole first workload: 1M parameters, 2 ranks, Inf in step 2
+    "cfg1": CFG1,
+    # GPT-2-shaped list, 8 ranks, bf16, clip 1.0
+    "cfg2-small": CFG2.replace(numels=_small_gpt2(), steps=4),
+    # flat ragged vector, 16 ranks, fp16 x 2^12, dynamic scale, Inf every 2nd step
+    "cfg3-small": CFG3.replace(numels=(3_000_001,), steps=5, inject_every=2),
+    # rank 0 of 64, gradient buffers hold rank 0's slice only
+    "cfg4-small": CFG4.replace(numels=(64 * 50_000 + 13,), steps=3,
+                               inject_at=((2, 5, 1234),)),
+    # 8B-shaped list in buckets, 8 ranks, bf16, clip across buckets
+    "cfg5-small": CFG5.replace(numels=_small_decoder(), bucket=8 * 8 * 1000, steps=3),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_workload_lockstep(name):
+    wl = SMALL[name]
+    ls = Lockstep(wl)
+    for _ in range(wl.steps):
+        ls.step()
+        ls.check()
+    assert ls.st.t + ls.st.skipped == wl.steps
+
+
+@pytest.mark.parametrize("stage", [True, False])
+def test_clip_staged_and_recomputed_agree(stage):
+    """The two-pass clipped step gives the same bits whether the reduced
+    gradient is kept in fp32 between the passes or reduced again."""
+    wl = SMALL["cfg2-small"].replace(steps=2)
+    ls = Lockstep(wl, stage=stage)
+    for _ in range(2):
+        ls.step()
+        ls.check()
+
+
+EDGE = {
+    "one-rank": CFG1.replace(numels=(70_001,), world=1, steps=2, inject_at=()),
+    "three-ranks-generic": CFG1.replace(numels=(100_003, 17), world=3, steps=3,
+                                        inject_at=((2, 1, 50_000),)),
+    "hundred-ranks": CFG1.replace(numels=(100 * 640 + 8,), world=100, steps=2, inject_at=()),
+    "psi-below-world": CFG1.replace(numels=(5,), world=8, steps=2, inject_at=()),
+    "tiny-tensors-gaps": CFG2.replace(numels=(1, 2, 3, 65, 127, 4096, 7), world=4, steps=3),
+    "bf16-dynamic": CFG3.replace(numels=(200_000,), world=8, dtype=synth.BF16, steps=4,
+                                 inject_every=3),
+    "bucketed-rank-view": CFG5.replace(numels=_small_decoder(), bucket=8 * 8 * 1000, steps=2,
+                                       rank=5),
+    "bucketed-rank-slices": CFG5.replace(numels=_small_decoder(), bucket=8 * 8 * 1000,
+                                         steps=2, rank=3, grads_are_slices=True,
+                                         max_grad_norm=0.0),
+    "rank-view-full-buffers": CFG4.replace(numels=(16 * 4096 + 100,), world=16, rank=7,
+                                           grads_are_slices=False, steps=2),
+    "clip-never-active": CFG2.replace(numels=(50_000,), world=2, max_grad_norm=1e6, steps=2),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_lockstep(name):
+    wl = EDGE[name]
+    ls = Lockstep(wl)
+    for _ in range(wl.steps):
+        ls.step()
+        ls.check()
+
+
+@pytest.mark.parametrize("kw", [dict(adamw=False, weight_decay=0.05),
+                                dict(bias_correction=False),
+                                dict(dynamic_scale=True, growth_interval=2)],
+                         ids=["coupled-l2", "literal-adam", "scale-growth"])
+def test_optimizer_variants(kw):
+    wl = CFG1.replace(numels=(300_000,), steps=5, inject_at=((3, 1, 7),))
+    ls = Lockstep(wl, **kw)
+    for _ in range(wl.steps):
+        ls.step()
+        ls.check()
+
+
+@pytest.mark.parametrize("bits,where", [(0x7C00, "first"), (0xFC00, "boundary"),
+                                        (0x7E00, "last-real"), (0x7C01, "padding")])
+def test_overflow_anywhere_skips_bit_exactly(bits, where):
+    """NaN, +Inf or -Inf in any rank's buffer (first element, a partition
+    boundary, the last real element, a padding element) skips the step: the
+    current slot of every buffer is unchanged bit for bit."""
+    wl = CFG1.replace(numels=(100_001,), world=4, steps=2, inject_at=(), dtype=synth.F16,
+                      dynamic_scale=True)
+    ls = Lockstep(wl)
+    ls.step()
+    ls.check()
+    before = [t.clone() for t in ls.z.current()]
+    g = gen_grads(wl, ls.lay, 2, ls.st.loss_scale)
+    P = ls.lay.owned
+    pos = {"first": (0, 0), "boundary": (2, 2 * P - 1), "last-real": (3, 100_000),
+           "padding": (1, ls.lay.padded - 1)}[where]
+    g[pos[0]][pos[1]] = bits
+    ls.step(g)
+    st = ls.check()
+    assert st.overflow == 1 and st.t == 1 and st.loss_scale == wl.loss_scale / 2
+    for a, b in zip(before, ls.z.current()):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.float32 else a.view(torch.int32),
+                           b.view(torch.uint8) if b.dtype != torch.float32 else b.view(torch.int32))
+
+
+def test_empty_vector():
+    cfg = zs.adam_cfg()
+    z = zs.ZeroStep((), 4, synth.F16, cfg)
+    assert z.layout.padded_numel == 0
+    grads = [torch.empty(0, dtype=torch.float16, device="cuda") for _ in range(4)]
+    z.step(grads)
+    torch.cuda.synchronize()
+    st = z.read_state()
+    assert st.t == 1 and st.overflow == 0
+
+
+def test_unfused_entry_points_match_oracle_and_fused():
+    """reduce-scatter -> overflow check -> norm -> Adam -> finalize through the
+    separate entry points: the reduced gradient is bit-exact, the norm within
+    tolerance, and the result equals the fused step's."""
+    wl = CFG2.replace(numels=(123_457, 999), world=8, steps=1)
+    lay = oracle.layout(wl.numels, wl.world)
+    zl, _ = zs.zero_partition_layout(wl.numels, wl.world)
+    grads = gen_grads(wl, lay, 1, 1.0)
+    gd = [to_dev_half(g, wl.dtype) for g in grads]
+    dev = "cuda"
+    # (a2) all ranks and one rank
+    g_all = torch.empty(lay.padded, dtype=torch.float32, device=dev)
+    zs.zero_reduce_scatter_sum(gd, zl, g_all)
+    want = oracle.reduce_sum(grads, wl.dtype, 0, lay.padded)
+    assert np.array_equal(g_all.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    g3 = torch.empty(lay.owned, dtype=torch.float32, device=dev)
+    zs.zero_reduce_scatter_sum(gd, zl, g3, rank=3)
+    assert np.array_equal(g3.cpu().numpy(), want[rank_index(lay, 3)])
+    # (a4)
+    state = zs.new_state(1.0)
+    zs.zero_check_overflow(g_all, 1.0, zs.state_field_ptr(state, "found_inf"))
+    assert zs.read_state(state).found_inf == 0
+    bad = g_all.clone()
+    bad[lay.padded - 1] = float("nan")
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    zs.zero_check_overflow(bad, 1.0, flag.data_ptr())
+    assert int(flag.item()) == 1
+    odd = g_all[:13].clone()
+    odd[12] = float("-inf")
+    flag.zero_()
+    zs.zero_check_overflow(odd, 1.0, flag.data_ptr())
+    assert int(flag.item()) == 1
+    # (a5)
+    ws = torch.empty(zs.zero_workspace_bytes(wl.world), dtype=torch.uint8, device=dev)
+    zs.zero_grad_norm(g_all, 1.0, zs.state_field_ptr(state, "sumsq"), ws)
+    s = zs.read_state(state).sumsq
+    ref = oracle.sumsq(want)
+    assert abs(s - ref) <= 1e-12 * ref
+    for n in (0, 1, 7, 9, 1001):
+        out = torch.zeros(1, dtype=torch.float64, device=dev)
+        zs.zero_grad_norm(g_all[:n].clone(), 0.5, out.data_ptr(), ws)
+        h = want[:n].copy()
+        oracle.unscale(h, 0.5)
+        r = oracle.sumsq(h)
+        assert abs(float(out.item()) - r) <= 1e-12 * max(r, 1e-300)
+    # (a6)-(a8) with the clip
+    cfg = lib_cfg(wl)
+    master = gen_master_flat(wl, lay)
+    w = torch.from_numpy(master.copy()).to(dev)
+    m = torch.zeros_like(w)
+    v = torch.zeros_like(w)
+    out = torch.empty(lay.padded, dtype=zs.torch_dtype(wl.dtype), device=dev)
+    zs.zero_adam_step(g_all, w, m, v, out, cfg, state)
+    zs.zero_step_finalize(cfg, state)
+    torch.cuda.synchronize()
+    ost = oracle.State()
+    wo, mo, vo = master.copy(), np.zeros_like(master), np.zeros_like(master)
+    ho = np.zeros(lay.padded, np.uint16)
+    oracle.step(grads, wl.dtype, lay, oracle_cfg(wl), ost, wo, mo, vo, ho)
+    assert_close("master", w.cpu().numpy(), wo)
+    assert_close("m", m.cpu().numpy(), mo)
+    assert_close("v", v.cpu().numpy(), vo)
+    st = zs.read_state(state)
+    assert st.t == 1 and st.cur == 0
+    # the fused step gives the same bits when its clip coefficient (from a
+    # per-rank norm) rounds to the same binary32 value
+    ls = Lockstep(wl)
+    ls.step(grads)
+    fst = ls.check()
+    fw, fm, fv, fp = ls.z.current()
+    if fst.clip_coef == oracle.clip_coef(s, wl.max_grad_norm):
+        assert torch.equal(fw.view(torch.int32), w.view(torch.int32))
+        assert torch.equal(fv.view(torch.int32), v.view(torch.int32))
+        assert np.array_equal(half_bits(fp), half_bits(out))
+
+
+def gen_master_flat(wl, lay):
+    from zs_harness import gen_master
+    return gen_master(wl, lay)
+
+
+def test_adam_step_skips_on_flag_and_tail():
+    """zero_adam_step changes nothing when the state's flag is set, and
+    handles a length that is not a multiple of 8."""
+    n = 1003
+    dev = "cuda"
+    g = torch.randn(n, device=dev) * 1e-3
+    w0 = torch.randn(n, device=dev) * 0.02
+    w, m, v = w0.clone(), torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    out = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    cfg = zs.adam_cfg(weight_decay=0.01)
+    state = zs.new_state(1.0)
+    off = zs.StepState.found_inf.offset
+    state[off:off + 4].copy_(torch.ones(1, dtype=torch.int32, device=dev).view(torch.uint8))
+    zs.zero_adam_step(g, w, m, v, out, cfg, state)
+    torch.cuda.synchronize()
+    assert torch.equal(w, w0) and not m.any() and not out.view(torch.int16).any()
+    zs.zero_step_finalize(cfg, state)
+    st = zs.read_state(state)
+    assert st.overflow == 1 and st.t == 0 and st.found_inf == 0
+    zs.zero_adam_step(g, w, m, v, out, cfg, state)
+    torch.cuda.synchronize()
+    sc = oracle.step_scalars(oracle.AdamCfg(weight_decay=0.01), oracle.State())
+    wo, mo, vo = w0.cpu().numpy().copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adam(g.cpu().numpy().copy(), wo, mo, vo, sc)
+    assert_close("master", w.cpu().numpy(), wo)
+    assert np.array_equal(half_bits(out), oracle.f32_to_half(wo, oracle.BF16))
+
+
+def test_generators_agree():
+    """The GPU input generator gives the CPU generator's bits."""
+    dev = "cuda"
+    for dtype in (synth.F16, synth.BF16):
+        k = synth.key(1234, 5)
+        n = 100_003
+        cpu = synth.fill_half(k, 777, n, 4.1, dtype)
+        gpu = torch.empty(n, dtype=torch.int16, device=dev)
+        synth.gpu_fill_half(k, 777, gpu, 4.1, dtype)
+        assert np.array_equal(gpu.cpu().numpy().view(np.uint16), cpu)
+    k = synth.key(99, 10_000)
+    cpu = synth.fill_f32(k, 0, 50_001, 0.02)
+    gpu = torch.empty(50_001, dtype=torch.float32, device=dev)
+    synth.gpu_fill_f32(k, 0, gpu, 0.02)
+    assert np.array_equal(gpu.cpu().numpy().view(np.uint32), cpu.view(np.uint32))
+    x = torch.randn(4099, device=dev) * 100
+    for dtype in (synth.F16, synth.BF16):
+        out = torch.empty(4099, dtype=torch.int16, device=dev)
+        synth.gpu_round_half(x, out, dtype)
+        assert np.array_equal(out.cpu().numpy().view(np.uint16),
+                              synth.round_half(x.cpu().numpy(), dtype))

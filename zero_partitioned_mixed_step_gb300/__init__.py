@@ -1,0 +1,236 @@
+"""GB300-native partitioned mixed-precision ZeRO Adam step.
+
+A thin Python binding of ``libzerostep.so`` (C ABI declared in
+``include/zerostep.h``): the functions below only marshal arguments; every
+step of the computation runs in the library's sm_103a kernels.  PyTorch is
+used for device memory, streams and pinned host memory.
+
+Entry points (same names as the C ABI):
+  zero_partition_layout, zero_state_init, zero_workspace_bytes,
+  zero_reduce_scatter_sum, zero_check_overflow, zero_grad_norm,
+  zero_adam_step, zero_step_finalize, zero_step_fused.
+``ZeroStep`` owns the buffers of one simulated data-parallel group and runs
+the fused step on them.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+from ._abi import (BF16, F16, MAX_WORLD, AdamCfg, Layout, StepState, ZeroError, check, lib)
+
+__all__ = [
+    "F16", "BF16", "MAX_WORLD", "AdamCfg", "Layout", "StepState", "ZeroError", "ZeroStep",
+    "adam_cfg", "new_state", "read_state", "state_field_ptr", "zero_partition_layout",
+    "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
+    "zero_grad_norm", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
+]
+
+_TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"half-precision tensor expected, got {t.dtype}")
+
+
+def torch_dtype(code: int) -> torch.dtype:
+    return _TORCH_DT[code]
+
+
+def _dev_ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("contiguous CUDA tensor expected")
+    return t.data_ptr()
+
+
+def _ptr_array(tensors: Sequence[torch.Tensor]):
+    return (ctypes.c_void_p * len(tensors))(*[_dev_ptr(t) for t in tensors])
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# ----------------------------------------------------------------- host helpers
+
+def zero_partition_layout(numels: Sequence[int], world: int, align_elems: int = 64,
+                          bucket_numel: int = 0) -> Tuple[Layout, List[int]]:
+    """Step (a1).  Returns the layout and every tensor's flat offset."""
+    n = len(numels)
+    arr = (ctypes.c_int64 * max(n, 1))(*numels)
+    offs = (ctypes.c_int64 * max(n, 1))()
+    out = Layout()
+    check("zero_partition_layout",
+          lib().zero_partition_layout(n, arr, world, align_elems, bucket_numel, offs,
+                                      ctypes.byref(out)))
+    return out, list(offs[:n])
+
+
+def zero_state_init(loss_scale: float = 1.0) -> StepState:
+    s = StepState()
+    check("zero_state_init", lib().zero_state_init(ctypes.byref(s), loss_scale))
+    return s
+
+
+def zero_workspace_bytes(world: int) -> int:
+    n = lib().zero_workspace_bytes(world)
+    if n == 0:
+        raise ZeroError("zero_workspace_bytes", -1)
+    return n
+
+
+def adam_cfg(lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+             weight_decay: float = 0.0, adamw: bool = True, bias_correction: bool = True,
+             max_grad_norm: float = 0.0, dynamic_scale: bool = False, growth_interval: int = 1000,
+             backoff: float = 0.5, growth: float = 2.0, min_scale: float = 1.0) -> AdamCfg:
+    return AdamCfg(lr, beta1, beta2, eps, weight_decay, int(adamw), int(bias_correction),
+                   max_grad_norm, int(dynamic_scale), growth_interval, backoff, growth, min_scale)
+
+
+def new_state(loss_scale: float = 1.0, device="cuda") -> torch.Tensor:
+    """A device-resident zero_step_state (64 bytes) in its initial state."""
+    s = zero_state_init(loss_scale)
+    host = torch.frombuffer(bytearray(bytes(s)), dtype=torch.uint8)
+    return host.to(device)
+
+
+def read_state(state: torch.Tensor) -> StepState:
+    """Copy a device state to the host (synchronises with its stream)."""
+    return StepState.from_buffer_copy(bytes(state.cpu().numpy().tobytes()))
+
+
+def state_field_ptr(state: torch.Tensor, field: str) -> int:
+    return state.data_ptr() + getattr(StepState, field).offset
+
+
+# ----------------------------------------------------------------- device entry points
+
+def zero_reduce_scatter_sum(grads: Sequence[torch.Tensor], layout: Layout, g_out: torch.Tensor,
+                            rank: int = -1, grads_are_slices: bool = False, stream=None) -> None:
+    check("zero_reduce_scatter_sum",
+          lib().zero_reduce_scatter_sum(_ptr_array(grads), int(grads_are_slices),
+                                        _dtype_code(grads[0]), ctypes.byref(layout), rank,
+                                        _dev_ptr(g_out), _stream(stream)))
+
+
+def zero_check_overflow(g: torch.Tensor, inv_scale: float, flag_ptr: int, stream=None) -> None:
+    check("zero_check_overflow",
+          lib().zero_check_overflow(_dev_ptr(g), g.numel(), inv_scale, flag_ptr, _stream(stream)))
+
+
+def zero_grad_norm(g: torch.Tensor, inv_scale: float, sumsq_ptr: int, ws: torch.Tensor,
+                   stream=None) -> None:
+    check("zero_grad_norm",
+          lib().zero_grad_norm(_dev_ptr(g), g.numel(), inv_scale, sumsq_ptr, _dev_ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def zero_adam_step(g: torch.Tensor, master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
+                   half_out: torch.Tensor, cfg: AdamCfg, state: torch.Tensor, stream=None) -> None:
+    check("zero_adam_step",
+          lib().zero_adam_step(_dev_ptr(g), _dev_ptr(master), _dev_ptr(m), _dev_ptr(v),
+                               _dev_ptr(half_out), _dtype_code(half_out), g.numel(),
+                               ctypes.byref(cfg), _dev_ptr(state), _stream(stream)))
+
+
+def zero_step_finalize(cfg: AdamCfg, state: torch.Tensor, flip_slot: bool = False,
+                       stream=None) -> None:
+    check("zero_step_finalize",
+          lib().zero_step_finalize(ctypes.byref(cfg), _dev_ptr(state), int(flip_slot),
+                                   _stream(stream)))
+
+
+def zero_step_fused(grads: Sequence[torch.Tensor], layout: Layout,
+                    master: Sequence[torch.Tensor], m: Sequence[torch.Tensor],
+                    v: Sequence[torch.Tensor], params: Sequence[torch.Tensor], cfg: AdamCfg,
+                    state: torch.Tensor, ws: torch.Tensor, rank: int = -1,
+                    g_stage: Optional[torch.Tensor] = None, grads_are_slices: bool = False,
+                    stream=None) -> None:
+    """The whole step (a2)-(a8).  master, m, v and params are the two
+    ping-pong slots (the same tensor twice for an in-place clipped step)."""
+    check("zero_step_fused",
+          lib().zero_step_fused(_ptr_array(grads), int(grads_are_slices), _dtype_code(grads[0]),
+                                ctypes.byref(layout), rank, _ptr_array(master), _ptr_array(m),
+                                _ptr_array(v), _ptr_array(params), _dev_ptr(g_stage),
+                                ctypes.byref(cfg), _dev_ptr(state), _dev_ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ----------------------------------------------------------------- buffer owner
+
+class ZeroStep:
+    """The buffers of one simulated data-parallel group and its fused step.
+
+    rank = -1 simulates every rank (state buffers span the padded flat
+    vector); rank = r simulates rank r alone (state buffers hold r's owned
+    elements).  Without clipping the master/m/v/params buffers are
+    double-buffered so an overflow step can be skipped in one pass; with
+    clipping they are updated in place and the reduced gradient is staged in
+    fp32 between the two passes when that reads fewer bytes (N_d > 4).
+    """
+
+    def __init__(self, numels: Sequence[int], world: int, dtype: int, cfg: AdamCfg,
+                 loss_scale: float = 1.0, rank: int = -1, bucket_numel: int = 0,
+                 align_elems: int = 64, grads_are_slices: bool = False,
+                 stage_grad: Optional[bool] = None, device="cuda"):
+        self.layout, self.offsets = zero_partition_layout(numels, world, align_elems, bucket_numel)
+        self.world, self.dtype, self.cfg, self.rank = world, dtype, cfg, rank
+        self.grads_are_slices = grads_are_slices
+        L = self.layout
+        self.n_state = L.padded_numel if rank < 0 else L.owned_numel
+        clip = cfg.max_grad_norm > 0
+        hdt = torch_dtype(dtype)
+        f32 = dict(dtype=torch.float32, device=device)
+        slots = 1 if clip else 2
+        self.master = [torch.zeros(self.n_state, **f32) for _ in range(slots)]
+        self.m = [torch.zeros(self.n_state, **f32) for _ in range(slots)]
+        self.v = [torch.zeros(self.n_state, **f32) for _ in range(slots)]
+        self.params = [torch.zeros(L.padded_numel, dtype=hdt, device=device) for _ in range(slots)]
+        if slots == 1:
+            for lst in (self.master, self.m, self.v, self.params):
+                lst.append(lst[0])
+        if stage_grad is None:
+            stage_grad = clip and world > 4
+        self.g_stage = torch.empty(self.n_state, **f32) if (clip and stage_grad) else None
+        self.state = new_state(loss_scale, device)
+        self.ws = torch.empty(zero_workspace_bytes(world), dtype=torch.uint8, device=device)
+
+    def grad_numel(self) -> int:
+        """Elements of each rank's gradient buffer."""
+        return self.layout.owned_numel if self.grads_are_slices else self.layout.padded_numel
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None) -> None:
+        zero_step_fused(grads, self.layout, self.master, self.m, self.v, self.params, self.cfg,
+                        self.state, self.ws, self.rank, self.g_stage, self.grads_are_slices,
+                        stream)
+
+    def step_from_host(self, host_grads: Sequence[torch.Tensor],
+                       device_grads: Sequence[torch.Tensor], stream=None) -> StepState:
+        """End to end: copy each rank's gradient from (pinned) host memory,
+        run the step and read the step state back to the host."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            for h, d in zip(host_grads, device_grads):
+                d.copy_(h, non_blocking=True)
+            self.step(device_grads, s)
+            out = torch.empty(64, dtype=torch.uint8, pin_memory=True)
+            out.copy_(self.state, non_blocking=True)
+        s.synchronize()
+        return StepState.from_buffer_copy(bytes(out.numpy().tobytes()))
+
+    def read_state(self) -> StepState:
+        return read_state(self.state)
+
+    def current(self):
+        """(master, m, v, params) of the slot holding the current state."""
+        c = self.read_state().cur
+        return self.master[c], self.m[c], self.v[c], self.params[c]

@@ -1,0 +1,290 @@
+// The unfused entry points (zero_check_overflow, zero_grad_norm,
+// zero_adam_step, zero_step_finalize) and the small single-CTA kernels that
+// end a step.
+#include <cmath>
+
+#include "kernels.cuh"
+
+namespace zs {
+
+int target_ctas(const void *kernel)
+{
+    int dev = 0, sms = 0, occ = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+        occ < 1)
+        occ = 1;
+    const int64_t t = (int64_t)sms * occ;
+    return (int)(t > kMaxCtas ? kMaxCtas : t);
+}
+
+// ------------------------------------------------------------------ end of step
+
+struct FinCfg {
+    double beta1, beta2, backoff, growth, min_scale;
+    int32_t dynamic, interval;
+};
+
+__global__ void finalize_kernel(FinCfg c, zero_step_state *st, int flip)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0)
+        return;
+    if (st->found_inf) {
+        st->overflow = 1;
+        st->skipped += 1;
+        if (c.dynamic) {
+            const double s = __dmul_rn((double)st->loss_scale, c.backoff);
+            st->loss_scale = __double2float_rn(s > c.min_scale ? s : c.min_scale);
+            st->good_steps = 0;
+        }
+    } else {
+        st->overflow = 0;
+        st->t += 1;
+        st->beta1_pow = __dmul_rn(st->beta1_pow, c.beta1);
+        st->beta2_pow = __dmul_rn(st->beta2_pow, c.beta2);
+        if (flip)
+            st->cur ^= 1;
+        st->good_steps += 1;
+        if (c.dynamic && st->good_steps == c.interval) {
+            st->loss_scale = __double2float_rn(__dmul_rn((double)st->loss_scale, c.growth));
+            st->good_steps = 0;
+        }
+    }
+    st->found_inf = 0;
+}
+
+int launch_finalize(const zero_adam_cfg *cfg, zero_step_state *state, int flip, cudaStream_t s)
+{
+    FinCfg c{cfg->beta1, cfg->beta2, cfg->backoff, cfg->growth, cfg->min_scale,
+             cfg->dynamic_scale ? 1 : 0, cfg->growth_interval};
+    finalize_kernel<<<1, 32, 0, s>>>(c, state, flip);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+// Fixed-order reduction of per-CTA partials: warp w reduces rows w, w + 8, ...
+// (lane l adds columns l, l + 32, ... in order, then a fixed butterfly), then
+// thread 0 adds the row sums in row (rank) order.
+__global__ void __launch_bounds__(kThreads)
+    norm_finalize_kernel(const double *partials, int gx, int gy, double max_norm,
+                         zero_step_state *st, double *out)
+{
+    __shared__ double row_sum[ZERO_MAX_WORLD];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r < gy; r += kThreads / 32) {
+        double x = 0.0;
+        for (int i = lane; i < gx; i += 32)
+            x = __dadd_rn(x, partials[(int64_t)r * gx + i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+        if (lane == 0)
+            row_sum[r] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0)
+        return;
+    double total = 0.0;
+    for (int r = 0; r < gy; ++r)
+        total = __dadd_rn(total, row_sum[r]);
+    if (out)
+        *out = total;
+    if (st && !st->found_inf) {
+        st->sumsq = total;
+        if (max_norm > 0.0)
+            st->clip_coef = __double2float_rn(
+                fmin(1.0, __ddiv_rn(max_norm, __dadd_rn(__dsqrt_rn(total), 1e-6))));
+    }
+}
+
+int launch_norm_finalize(const double *partials, int gx, int gy, double max_norm,
+                         zero_step_state *state, double *out, cudaStream_t s)
+{
+    norm_finalize_kernel<<<1, kThreads, 0, s>>>(partials, gx, gy, max_norm, state, out);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+// ------------------------------------------------------------------ element-wise kernels
+
+static int grid_for(const void *kernel, int64_t units)
+{
+    const int target = target_ctas(kernel);
+    const int64_t want = (units + kThreads - 1) / kThreads;
+    return (int)(want < 1 ? 1 : (want < target ? want : target));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    overflow_kernel(const float *g, int64_t n, float inv_s, int32_t *flag)
+{
+    bool bad = false;
+    const int64_t n4 = n / 4;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < n4; k += stride) {
+        const float4 x = ld_state(g + 4 * k);
+        bad |= nonfinite(__fmul_rn(x.x, inv_s)) | nonfinite(__fmul_rn(x.y, inv_s)) |
+               nonfinite(__fmul_rn(x.z, inv_s)) | nonfinite(__fmul_rn(x.w, inv_s));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 3))
+        bad |= nonfinite(__fmul_rn(g[4 * n4 + threadIdx.x], inv_s));
+    flag_nonfinite(bad, flag);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    sumsq_kernel(const float *g, int64_t n, float inv_s, double *partials)
+{
+    SumSq ss;
+    const int64_t units = n / kUnit;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < units; k += stride) {
+        float x[8];
+        load8(g + k * kUnit, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            x[i] = __fmul_rn(x[i], inv_s);
+        ss.add8(x);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && (n % kUnit)) {
+        float x[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int64_t i = units * kUnit; i < n; ++i)
+            x[i - units * kUnit] = __fmul_rn(g[i], inv_s);
+        ss.add8(x);
+    }
+    const double tot = block_sum(ss.acc);
+    if (threadIdx.x == 0)
+        partials[blockIdx.x] = tot;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+    adam_kernel(const float *g, float *w, float *m, float *v, uint16_t *out, int64_t n,
+                CfgDev cfg, const zero_step_state *st)
+{
+    __shared__ Scalars sh;
+    if (threadIdx.x == 0)
+        compute_scalars(cfg, st, sh);
+    __syncthreads();
+    const Scalars s = sh;
+    if (s.skip)
+        return;
+    const bool scale = s.clip && s.coef < 1.0f;
+    const int64_t units = n / kUnit;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < units; k += stride) {
+        const int64_t e = k * kUnit;
+        float gg[8], ww[8], mm[8], vv[8];
+        load8(g + e, gg);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            gg[i] = __fmul_rn(gg[i], s.inv_s);
+            if (scale)
+                gg[i] = __fmul_rn(gg[i], s.coef);
+        }
+        load8(w + e, ww);
+        load8(m + e, mm);
+        load8(v + e, vv);
+        adam8(gg, ww, mm, vv, s);
+        store8(w + e, ww);
+        store8(m + e, mm);
+        store8(v + e, vv);
+        st_half8(out + e, pack_half8<DT>(ww));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n % kUnit)) {
+        const int64_t e = units * kUnit + threadIdx.x;
+        float gg = __fmul_rn(g[e], s.inv_s);
+        if (scale)
+            gg = __fmul_rn(gg, s.coef);
+        float ww = w[e], mm = m[e], vv = v[e];
+        adam1(gg, ww, mm, vv, s);
+        w[e] = ww;
+        m[e] = mm;
+        v[e] = vv;
+        out[e] = round_half1<DT>(ww);
+    }
+}
+
+}  // namespace zs
+
+using namespace zs;
+
+extern "C" {
+
+int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *flag_dev,
+                        zero_stream_t stream)
+{
+    if (n < 0 || !flag_dev || (n > 0 && !g) || !(inv_scale > 0.0f) || !std::isfinite(inv_scale))
+        return ZERO_EINVAL;
+    if (!aligned16(g) || (reinterpret_cast<uintptr_t>(flag_dev) & 3u))
+        return ZERO_EALIGN;
+    if (n == 0)
+        return ZERO_OK;
+    const int gx = grid_for(reinterpret_cast<const void *>(overflow_kernel), n / 4);
+    overflow_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, flag_dev);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
+                   size_t ws_bytes, zero_stream_t stream)
+{
+    if (n < 0 || !sumsq_dev || !ws || (n > 0 && !g) || !(inv_scale > 0.0f) ||
+        !std::isfinite(inv_scale))
+        return ZERO_EINVAL;
+    if (!aligned16(g) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(sumsq_dev) & 7u))
+        return ZERO_EALIGN;
+    if (ws_bytes < zero_workspace_bytes(1))
+        return ZERO_ESPACE;
+    double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
+    const int gx = grid_for(reinterpret_cast<const void *>(sumsq_kernel), n / kUnit);
+    sumsq_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, partials);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_error(e);
+    return launch_norm_finalize(partials, gx, 1, 0.0, nullptr, sumsq_dev, stream);
+}
+
+int zero_adam_step(const float *g, float *master, float *m, float *v, void *half_out,
+                   zero_dtype dtype, int64_t n, const zero_adam_cfg *cfg,
+                   const zero_step_state *state_dev, zero_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if (n < 0 || !state_dev || (dtype != ZERO_F16 && dtype != ZERO_BF16) ||
+        (n > 0 && (!g || !master || !m || !v || !half_out)))
+        return ZERO_EINVAL;
+    if (!aligned16(g) || !aligned16(master) || !aligned16(m) || !aligned16(v) ||
+        !aligned16(half_out) || (reinterpret_cast<uintptr_t>(state_dev) & 7u))
+        return ZERO_EALIGN;
+    if (n == 0)
+        return ZERO_OK;
+    const CfgDev c{cfg->lr, cfg->beta1, cfg->beta2, cfg->eps, cfg->weight_decay,
+                   cfg->max_grad_norm, cfg->adamw ? 1 : 0, cfg->bias_correction ? 1 : 0};
+    uint16_t *out = static_cast<uint16_t *>(half_out);
+    if (dtype == ZERO_F16) {
+        const int gx = grid_for(reinterpret_cast<const void *>(adam_kernel<ZERO_F16>), n / kUnit);
+        adam_kernel<ZERO_F16><<<gx, kThreads, 0, stream>>>(g, master, m, v, out, n, c, state_dev);
+    } else {
+        const int gx = grid_for(reinterpret_cast<const void *>(adam_kernel<ZERO_BF16>), n / kUnit);
+        adam_kernel<ZERO_BF16><<<gx, kThreads, 0, stream>>>(g, master, m, v, out, n, c, state_dev);
+    }
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int flip_slot,
+                       zero_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if (!state_dev)
+        return ZERO_EINVAL;
+    if (reinterpret_cast<uintptr_t>(state_dev) & 7u)
+        return ZERO_EALIGN;
+    return launch_finalize(cfg, state_dev, flip_slot ? 1 : 0, stream);
+}
+
+}  // extern "C"

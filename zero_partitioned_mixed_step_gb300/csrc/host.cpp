@@ -1,0 +1,144 @@
+// Host-only entry points: the partition layout (step a1), the initial step
+// state, the workspace size and the error strings.
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+namespace zs {
+
+static int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int check_layout(const zero_layout *lay)
+{
+    if (!lay || lay->world < 1 || lay->world > ZERO_MAX_WORLD || lay->align_elems < 8 ||
+        lay->align_elems % 8 || lay->padded_numel < 0 || lay->owned_numel < 0)
+        return ZERO_EINVAL;
+    const int64_t w = lay->world;
+    if (lay->owned_numel * w != lay->padded_numel || lay->padded_numel % (w * 8))
+        return ZERO_EINVAL;
+    if (lay->bucket_numel == 0) {
+        if (lay->slice_numel != lay->owned_numel || lay->last_slice_numel != lay->owned_numel)
+            return ZERO_EINVAL;
+        return ZERO_OK;
+    }
+    if (lay->bucket_numel < 0 || lay->bucket_numel % (w * 8) || lay->num_buckets < 0 ||
+        lay->slice_numel * w != lay->bucket_numel || lay->last_slice_numel % 8)
+        return ZERO_EINVAL;
+    if (lay->num_buckets == 0)
+        return lay->padded_numel == 0 ? ZERO_OK : ZERO_EINVAL;
+    if ((lay->num_buckets - 1) * lay->slice_numel + lay->last_slice_numel != lay->owned_numel)
+        return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+static bool power_of_two(double x)
+{
+    int e;
+    return x > 0.0 && std::isfinite(x) && std::frexp(x, &e) == 0.5;
+}
+
+int check_cfg(const zero_adam_cfg *c)
+{
+    if (!c)
+        return ZERO_EINVAL;
+    if (!(c->lr >= 0.0) || !(c->beta1 >= 0.0 && c->beta1 < 1.0) ||
+        !(c->beta2 >= 0.0 && c->beta2 < 1.0) || !(c->eps > 0.0) || !(c->weight_decay >= 0.0) ||
+        !(c->max_grad_norm >= 0.0) || !std::isfinite(c->max_grad_norm))
+        return ZERO_EINVAL;
+    // powers of two keep the loss scale, and so the unscale, exact
+    if (c->dynamic_scale &&
+        (c->growth_interval < 1 || !(c->backoff <= 1.0) || !power_of_two(c->backoff) ||
+         !(c->growth >= 1.0) || !power_of_two(c->growth) || !power_of_two(c->min_scale)))
+        return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+}  // namespace zs
+
+extern "C" {
+
+const char *zero_strerror(int code)
+{
+    switch (code) {
+    case ZERO_OK: return "ok";
+    case ZERO_EINVAL: return "invalid argument";
+    case ZERO_EALIGN: return "buffer not 16-byte aligned";
+    case ZERO_ESPACE: return "workspace too small";
+    default: return code <= ZERO_ECUDA_BASE ? "CUDA launch failed" : "unknown error";
+    }
+}
+
+int zero_version(void) { return 1; }
+
+int zero_partition_layout(int n_tensors, const int64_t *numel, int world, int align_elems,
+                          int64_t bucket_numel, int64_t *tensor_offset_out, zero_layout *out)
+{
+    if (!out || n_tensors < 0 || (n_tensors > 0 && !numel) || world < 1 ||
+        world > ZERO_MAX_WORLD || align_elems < 8 || align_elems % 8 || bucket_numel < 0 ||
+        (bucket_numel > 0 && bucket_numel % ((int64_t)world * 8)))
+        return ZERO_EINVAL;
+    const int64_t limit = INT64_C(1) << 52;  // keeps every derived size far from overflow
+    int64_t off = 0, total = 0;
+    for (int k = 0; k < n_tensors; ++k) {
+        if (numel[k] < 0 || numel[k] > limit)
+            return ZERO_EINVAL;
+        off = zs::round_up(off, align_elems);
+        if (tensor_offset_out)
+            tensor_offset_out[k] = off;
+        off += numel[k];
+        total += numel[k];
+        if (off > limit)
+            return ZERO_EINVAL;
+    }
+    zero_layout L;
+    std::memset(&L, 0, sizeof L);
+    L.numel = total;
+    L.flat_numel = off;
+    L.world = world;
+    L.align_elems = align_elems;
+    L.bucket_numel = bucket_numel;
+    const int64_t unit = (int64_t)world * align_elems;
+    if (bucket_numel == 0) {
+        L.padded_numel = zs::round_up(off, unit);
+        L.owned_numel = L.padded_numel / world;
+        L.num_buckets = L.padded_numel ? 1 : 0;
+        L.slice_numel = L.last_slice_numel = L.owned_numel;
+    } else {
+        L.slice_numel = bucket_numel / world;
+        if (off > 0) {
+            L.num_buckets = (off + bucket_numel - 1) / bucket_numel;
+            const int64_t last = off - (L.num_buckets - 1) * bucket_numel;
+            const int64_t last_pad = zs::round_up(last, unit);
+            L.padded_numel = (L.num_buckets - 1) * bucket_numel + last_pad;
+            L.last_slice_numel = last_pad / world;
+            L.owned_numel = (L.num_buckets - 1) * L.slice_numel + L.last_slice_numel;
+        }
+    }
+    *out = L;
+    return ZERO_OK;
+}
+
+int zero_state_init(zero_step_state *s, float loss_scale)
+{
+    if (!s || !(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+        return ZERO_EINVAL;
+    int e;
+    if (std::frexp(loss_scale, &e) != 0.5f)  // a power of two keeps 1/S exact
+        return ZERO_EINVAL;
+    std::memset(s, 0, sizeof *s);
+    s->beta1_pow = 1.0;
+    s->beta2_pow = 1.0;
+    s->loss_scale = loss_scale;
+    s->clip_coef = 1.0f;
+    return ZERO_OK;
+}
+
+size_t zero_workspace_bytes(int world)
+{
+    if (world < 1 || world > ZERO_MAX_WORLD)
+        return 0;
+    return (size_t)zs::kWsHeader + sizeof(double) * (size_t)(zs::kMaxCtas + 2 * world);
+}
+
+}  // extern "C"

@@ -1,0 +1,328 @@
+// Device helpers of the step kernels: 16-byte loads and stores, the
+// rank-ordered reduction of one 8-element unit, the per-step scalars, the
+// Adam update, the round-to-nearest-even cast and the deterministic
+// sum-of-squares reduction.
+//
+// Arithmetic conventions (they make the GPU results reproduce the CPU
+// oracle's bits): every binary32 operation is an explicitly rounded
+// intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn ...), so nothing is
+// contracted into a fused multiply-add; per-step scalars are computed in
+// binary64 with IEEE division and square root and rounded once to binary32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace zs {
+
+// ------------------------------------------------------------------ memory
+
+// Gradient streams are read once: non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Optimizer state may be updated in place by the same thread, so it is read
+// through the coherent path (evict-first).
+__device__ __forceinline__ float4 ld_state(const float *p)
+{
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+
+__device__ __forceinline__ void st_state(float *p, float4 v)
+{
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+
+__device__ __forceinline__ void st_half8(uint16_t *p, uint4 v)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+// ------------------------------------------------------------------ conversions
+
+// Add the 8 half-precision values of x (exactly converted to fp32) to acc.
+template <int DT>
+__device__ __forceinline__ void add_half8(float acc[8], const uint4 x)
+{
+    const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float lo, hi;
+        if constexpr (DT == ZERO_F16) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&u[j]);
+            float2 f = __half22float2(h);
+            lo = f.x;
+            hi = f.y;
+        } else {
+            lo = __uint_as_float(u[j] << 16);
+            hi = __uint_as_float(u[j] & 0xFFFF0000u);
+        }
+        acc[2 * j] = __fadd_rn(acc[2 * j], lo);
+        acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], hi);
+    }
+}
+
+// Round 8 fp32 values to half precision, nearest even, packed little-endian.
+template <int DT>
+__device__ __forceinline__ uint4 pack_half8(const float w[8])
+{
+    uint32_t u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (DT == ZERO_F16) {
+            __half2 h = __floats2half2_rn(w[2 * j], w[2 * j + 1]);
+            u[j] = *reinterpret_cast<uint32_t *>(&h);
+        } else {
+            __nv_bfloat162 b = __floats2bfloat162_rn(w[2 * j], w[2 * j + 1]);
+            u[j] = *reinterpret_cast<uint32_t *>(&b);
+        }
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+__device__ __forceinline__ bool nonfinite(float x)
+{
+    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+// ------------------------------------------------------------------ reduce-scatter
+
+template <int MAXW>
+struct GradTable {
+    const uint16_t *p[MAXW];
+};
+
+// acc[i] = sum over q of float(grads[q][gi + i]), i < 8, in ascending q from +0.
+// W > 0: the group size is known at compile time and loads are issued in
+// batches of up to 16 ranks before they are summed; W == 0: `world` at run time.
+template <int DT, int W, int MAXW>
+__device__ __forceinline__ void reduce_unit(const GradTable<MAXW> &t, int world, int64_t gi,
+                                            float acc[8])
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0.0f;
+    if constexpr (W > 0) {
+        constexpr int CH = W < 16 ? W : 16;
+#pragma unroll
+        for (int q0 = 0; q0 < W; q0 += CH) {
+            uint4 x[CH];
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                x[j] = ld_stream(t.p[q0 + j] + gi);
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                add_half8<DT>(acc, x[j]);
+        }
+    } else {
+        int q = 0;
+        for (; q + 8 <= world; q += 8) {
+            uint4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                x[j] = ld_stream(t.p[q + j] + gi);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                add_half8<DT>(acc, x[j]);
+        }
+        for (; q < world; ++q)
+            add_half8<DT>(acc, ld_stream(t.p[q] + gi));
+    }
+}
+
+// ------------------------------------------------------------------ element mapping
+
+// Which elements a launch covers.  A launch has gridDim.y ranks; the CTA row
+// y processes rank rank0 + y, walking that rank's owned units k = 0, 1, ...
+struct View {
+    int64_t owned_units;   // units each rank owns (owned_numel / 8)
+    int64_t part;          // owned_numel (flat stride between partitions, not bucketed)
+    int64_t bucket;        // elements per bucket, 0 = not bucketed
+    int64_t slice;         // a rank's elements in a full bucket
+    int64_t slice_units;   // slice / 8
+    int64_t full_units;    // units in the full buckets: (num_buckets - 1) * slice_units
+    int64_t last_base;     // flat start of the last bucket
+    int64_t last_slice;    // a rank's elements in the last bucket
+    int32_t rank0;
+    int32_t all_ranks;     // 1: state buffers are flat (state index = flat index)
+    int32_t grads_are_slices;
+    int32_t world;
+};
+
+__device__ __forceinline__ int64_t flat_of(const View &v, int r, int64_t k)
+{
+    const int64_t e = k * kUnit;
+    if (v.bucket == 0)
+        return (int64_t)r * v.part + e;
+    if (k < v.full_units) {
+        int64_t b;
+        if (v.full_units < (INT64_C(1) << 32))
+            b = (int64_t)((uint32_t)k / (uint32_t)v.slice_units);
+        else
+            b = k / v.slice_units;
+        return b * v.bucket + (int64_t)r * v.slice + (e - b * v.slice);
+    }
+    return v.last_base + (int64_t)r * v.last_slice + (e - v.full_units * kUnit);
+}
+
+// ------------------------------------------------------------------ per-step scalars
+
+struct CfgDev {
+    double lr, beta1, beta2, eps, wd, max_norm;
+    int32_t adamw, bias_correction;
+};
+
+struct Scalars {
+    float inv_s, b1, omb1, b2, omb2, step, rbc2, eps, decay, wd, coef;
+    int32_t adamw, clip, skip;
+};
+
+// Scalars of step t + 1 from the state at the start of the step.
+__device__ __forceinline__ void compute_scalars(const CfgDev &c, const zero_step_state *st,
+                                                Scalars &s)
+{
+    const double bp1 = __dmul_rn(st->beta1_pow, c.beta1);
+    const double bp2 = __dmul_rn(st->beta2_pow, c.beta2);
+    if (c.bias_correction) {
+        s.step = __double2float_rn(__ddiv_rn(c.lr, __dsub_rn(1.0, bp1)));
+        s.rbc2 = __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, bp2)));
+    } else {
+        s.step = __double2float_rn(c.lr);
+        s.rbc2 = 1.0f;
+    }
+    s.b1 = __double2float_rn(c.beta1);
+    s.omb1 = __double2float_rn(__dsub_rn(1.0, c.beta1));
+    s.b2 = __double2float_rn(c.beta2);
+    s.omb2 = __double2float_rn(__dsub_rn(1.0, c.beta2));
+    s.eps = __double2float_rn(c.eps);
+    s.decay = __double2float_rn(__dsub_rn(1.0, __dmul_rn(c.lr, c.wd)));
+    s.wd = __double2float_rn(c.wd);
+    s.adamw = c.adamw;
+    s.inv_s = __fdiv_rn(1.0f, st->loss_scale);
+    s.clip = c.max_norm > 0.0;
+    s.coef = 1.0f;
+    if (s.clip) {
+        const double n = __dsqrt_rn(st->sumsq);
+        s.coef = __double2float_rn(fmin(1.0, __ddiv_rn(c.max_norm, __dadd_rn(n, 1e-6))));
+    }
+    s.skip = st->found_inf;
+}
+
+// ------------------------------------------------------------------ Adam
+
+// One AdamW / Adam step on one element (binary32, each operation rounded):
+//   [coupled L2: g += wd w]
+//   m = b1 m + (1 - b1) g;  v = b2 v + (1 - b2) g^2
+//   [decoupled: w = w (1 - lr wd)]
+//   w = w - step * (m / (sqrt(v) / sqrt(1 - b2^t) + eps)),  step = lr / (1 - b1^t)
+__device__ __forceinline__ void adam1(float g, float &w, float &m, float &v, const Scalars &s)
+{
+    if (!s.adamw && s.wd != 0.0f)
+        g = __fadd_rn(g, __fmul_rn(s.wd, w));
+    const float mi = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    const float vi = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    float wi = s.adamw ? __fmul_rn(w, s.decay) : w;
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(vi), s.rbc2), s.eps);
+    wi = __fsub_rn(wi, __fmul_rn(s.step, __fdiv_rn(mi, den)));
+    m = mi;
+    v = vi;
+    w = wi;
+}
+
+__device__ __forceinline__ void adam8(const float g[8], float w[8], float m[8], float v[8],
+                                      const Scalars &s)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        adam1(g[i], w[i], m[i], v[i], s);
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t round_half1(float w)
+{
+    if constexpr (DT == ZERO_F16)
+        return __half_as_ushort(__float2half_rn(w));
+    else
+        return __bfloat16_as_ushort(__float2bfloat16_rn(w));
+}
+
+__device__ __forceinline__ void load8(const float *p, float x[8])
+{
+    const float4 a = ld_state(p), b = ld_state(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void store8(float *p, const float x[8])
+{
+    st_state(p, make_float4(x[0], x[1], x[2], x[3]));
+    st_state(p + 4, make_float4(x[4], x[5], x[6], x[7]));
+}
+
+// ------------------------------------------------------------------ sum of squares
+
+// Sum of squares beyond binary64 accuracy, without binary64 multiplies: each
+// square is split exactly into p + e (p = fl(g*g), e = fma(g, g, -p)); the
+// p of a unit are added with Knuth's TwoSum so their rounding errors are kept
+// too; the unit's (hi, lo) pair then enters a binary64 accumulator.
+struct SumSq {
+    double acc = 0.0;
+
+    __device__ __forceinline__ void add8(const float g[8])
+    {
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float p = __fmul_rn(g[i], g[i]);
+            const float e = __fmaf_rn(g[i], g[i], -p);
+            const float s = __fadd_rn(hi, p);
+            const float bb = __fsub_rn(s, hi);
+            const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+            hi = s;
+            lo = __fadd_rn(lo, __fadd_rn(err, e));
+        }
+        acc = __dadd_rn(acc, __dadd_rn((double)hi, (double)lo));
+    }
+};
+
+// Deterministic CTA sum of one double per thread: a fixed butterfly inside
+// each warp, then warp 0 adds the warp sums in warp order.  Valid in thread 0.
+__device__ __forceinline__ double block_sum(double x)
+{
+    __shared__ double warp_sums[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0)
+        warp_sums[warp] = x;
+    __syncthreads();
+    double total = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w)
+            total = __dadd_rn(total, warp_sums[w]);
+    }
+    return total;
+}
+
+// Report a non-finite gradient of this warp once.
+__device__ __forceinline__ void flag_nonfinite(bool bad, int32_t *flag)
+{
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0)
+        atomicOr(flag, 1);
+}
+
+}  // namespace zs

@@ -1,0 +1,343 @@
+// The streaming kernels of the step and the entry points zero_step_fused and
+// zero_reduce_scatter_sum.
+//
+// One kernel template covers the passes over the data.  Each thread handles
+// 8-element units (16-byte loads of each rank's half gradient, 32-byte loads
+// and stores of each fp32 state array), CTA row y walks rank rank0 + y's owned
+// units with a grid stride, and the grid is sized to fill every SM once.
+//   FUSED      (a2)-(a7) in one pass: reduce, unscale, flag, Adam from slot
+//              cur into slot 1 - cur, cast into the parameter buffer.
+//   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, per-CTA
+//              sums of squares, optionally keep g in a staging buffer.
+//   PASS2_*    (a5 clip)-(a7) of a clipped step, skipped when pass 1 flagged
+//              an overflow; g is reduced again or read from the stage.
+//   RS         (a2) alone: the reduced fp32 gradient.
+#include "kernels.cuh"
+
+namespace zs {
+
+enum Mode { M_FUSED = 0, M_PASS1 = 1, M_PASS2_RECOMPUTE = 2, M_PASS2_STAGED = 3, M_RS = 4 };
+
+template <int MAXW>
+struct StepParams {
+    GradTable<MAXW> grads;
+    View view;
+    CfgDev cfg;
+    zero_step_state *state;
+    const float *w0, *w1, *m0, *m1, *v0, *v1;  // ping-pong slots (reads)
+    float *wo0, *wo1, *mo0, *mo1, *vo0, *vo1;   // ping-pong slots (writes)
+    uint16_t *par0, *par1;                      // parameter buffer slots
+    float *stage;                               // PASS1 output / PASS2_STAGED input / RS output
+    double *partials;                           // PASS1: one per CTA
+};
+
+template <int DT, int W, int MAXW, int MODE>
+__global__ void __launch_bounds__(kThreads)
+    step_kernel(const __grid_constant__ StepParams<MAXW> p)
+{
+    __shared__ Scalars sh;
+    __shared__ int sh_cur;
+    Scalars s{};
+    int cur = 0;
+    if constexpr (MODE != M_RS) {
+        if (threadIdx.x == 0) {
+            compute_scalars(p.cfg, p.state, sh);
+            sh_cur = p.state->cur;
+        }
+        __syncthreads();
+        s = sh;
+        cur = sh_cur;
+        if constexpr (MODE == M_PASS2_RECOMPUTE || MODE == M_PASS2_STAGED) {
+            if (s.skip)
+                return;  // the whole step is skipped: write nothing
+        }
+    }
+    const View &vw = p.view;
+    const int r = vw.rank0 + (int)blockIdx.y;
+    const float *w_src = cur ? p.w1 : p.w0;
+    const float *m_src = cur ? p.m1 : p.m0;
+    const float *v_src = cur ? p.v1 : p.v0;
+    float *w_dst = cur ? p.wo0 : p.wo1;
+    float *m_dst = cur ? p.mo0 : p.mo1;
+    float *v_dst = cur ? p.vo0 : p.vo1;
+    uint16_t *out = cur ? p.par0 : p.par1;
+
+    bool bad = false;
+    SumSq ss;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < vw.owned_units; k += stride) {
+        const int64_t f = flat_of(vw, r, k);
+        const int64_t si = vw.all_ranks ? f : k * kUnit;
+        float g[8];
+        if constexpr (MODE == M_PASS2_STAGED) {
+            load8(p.stage + si, g);
+        } else {
+            const int64_t gi = vw.grads_are_slices ? k * kUnit : f;
+            reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g);
+            if constexpr (MODE == M_RS) {
+                store8(p.stage + si, g);
+                continue;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                g[i] = __fmul_rn(g[i], s.inv_s);
+        }
+        if constexpr (MODE == M_FUSED || MODE == M_PASS1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                bad |= nonfinite(g[i]);
+        }
+        if constexpr (MODE == M_PASS1) {
+            ss.add8(g);
+            if (p.stage)
+                store8(p.stage + si, g);
+            continue;
+        }
+        if constexpr (MODE == M_PASS2_RECOMPUTE || MODE == M_PASS2_STAGED) {
+            if (s.coef < 1.0f) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    g[i] = __fmul_rn(g[i], s.coef);
+            }
+        }
+        float w[8], m[8], v[8];
+        load8(w_src + si, w);
+        load8(m_src + si, m);
+        load8(v_src + si, v);
+        adam8(g, w, m, v, s);
+        store8(w_dst + si, w);
+        store8(m_dst + si, m);
+        store8(v_dst + si, v);
+        st_half8(out + f, pack_half8<DT>(w));
+    }
+    if constexpr (MODE == M_FUSED || MODE == M_PASS1)
+        flag_nonfinite(bad, &p.state->found_inf);
+    if constexpr (MODE == M_PASS1) {
+        const double tot = block_sum(ss.acc);
+        if (threadIdx.x == 0)
+            p.partials[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = tot;
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+template <int DT, int W, int MAXW, int MODE>
+int launch_one(const StepParams<MAXW> &p, int ranks, cudaStream_t stream, int *gx_out)
+{
+    auto kern = step_kernel<DT, W, MAXW, MODE>;
+    const int target = target_ctas(reinterpret_cast<const void *>(kern));
+    const int64_t want = (p.view.owned_units + kThreads - 1) / kThreads;
+    int64_t gx = (target + ranks - 1) / ranks;
+    if (want < gx)
+        gx = want;
+    if (gx < 1)
+        gx = 1;
+    if (gx_out)
+        *gx_out = (int)gx;
+    kern<<<dim3((unsigned)gx, (unsigned)ranks), kThreads, 0, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+template <int DT, int MAXW, int MODE>
+int dispatch_world(const StepParams<MAXW> &p, int ranks, cudaStream_t stream, int *gx)
+{
+    if constexpr (MODE == M_PASS2_STAGED) {
+        return launch_one<DT, 0, MAXW, MODE>(p, ranks, stream, gx);
+    } else if constexpr (MAXW == 64) {
+        switch (p.view.world) {
+        case 2: return launch_one<DT, 2, MAXW, MODE>(p, ranks, stream, gx);
+        case 4: return launch_one<DT, 4, MAXW, MODE>(p, ranks, stream, gx);
+        case 8: return launch_one<DT, 8, MAXW, MODE>(p, ranks, stream, gx);
+        case 16: return launch_one<DT, 16, MAXW, MODE>(p, ranks, stream, gx);
+        case 32: return launch_one<DT, 32, MAXW, MODE>(p, ranks, stream, gx);
+        case 64: return launch_one<DT, 64, MAXW, MODE>(p, ranks, stream, gx);
+        default: return launch_one<DT, 0, MAXW, MODE>(p, ranks, stream, gx);
+        }
+    } else {
+        return launch_one<DT, 0, MAXW, MODE>(p, ranks, stream, gx);
+    }
+}
+
+template <int MAXW>
+int dispatch(const StepParams<MAXW> &p, zero_dtype dt, int mode, int ranks, cudaStream_t s,
+             int *gx)
+{
+#define ZS_MODES(DT)                                                      \
+    switch (mode) {                                                       \
+    case M_FUSED: return dispatch_world<DT, MAXW, M_FUSED>(p, ranks, s, gx); \
+    case M_PASS1: return dispatch_world<DT, MAXW, M_PASS1>(p, ranks, s, gx); \
+    case M_PASS2_RECOMPUTE:                                               \
+        return dispatch_world<DT, MAXW, M_PASS2_RECOMPUTE>(p, ranks, s, gx); \
+    case M_PASS2_STAGED:                                                  \
+        return dispatch_world<DT, MAXW, M_PASS2_STAGED>(p, ranks, s, gx); \
+    default: return dispatch_world<DT, MAXW, M_RS>(p, ranks, s, gx);     \
+    }
+    if (dt == ZERO_F16) {
+        ZS_MODES(ZERO_F16)
+    } else {
+        ZS_MODES(ZERO_BF16)
+    }
+#undef ZS_MODES
+}
+
+// Everything a pass needs besides the per-mode pointers.
+struct PassArgs {
+    const void *const *grads;
+    int grads_are_slices;
+    zero_dtype dtype;
+    const zero_layout *lay;
+    int rank;
+    const zero_adam_cfg *cfg;
+    zero_step_state *state;
+    float *const *master, *const *m, *const *v;
+    void *const *params;
+    float *stage;
+    double *partials;
+};
+
+template <int MAXW>
+int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ranks_out)
+{
+    StepParams<MAXW> p{};
+    const zero_layout &L = *a.lay;
+    const int world = L.world;
+    if (a.grads)
+        for (int q = 0; q < world; ++q)
+            p.grads.p[q] = static_cast<const uint16_t *>(a.grads[q]);
+    View &v = p.view;
+    v.owned_units = L.owned_numel / kUnit;
+    v.part = L.owned_numel;
+    v.bucket = L.bucket_numel;
+    v.slice = L.slice_numel;
+    v.slice_units = L.slice_numel / kUnit;
+    v.full_units = L.bucket_numel ? (L.num_buckets - 1) * (L.slice_numel / kUnit) : 0;
+    v.last_base = L.bucket_numel ? (L.num_buckets - 1) * L.bucket_numel : 0;
+    v.last_slice = L.last_slice_numel;
+    v.rank0 = a.rank < 0 ? 0 : a.rank;
+    v.all_ranks = a.rank < 0;
+    v.grads_are_slices = a.grads_are_slices;
+    v.world = world;
+    if (a.cfg) {
+        const zero_adam_cfg &c = *a.cfg;
+        p.cfg = CfgDev{c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, c.max_grad_norm,
+                       c.adamw ? 1 : 0, c.bias_correction ? 1 : 0};
+    }
+    p.state = a.state;
+    if (a.master) {
+        p.w0 = p.wo0 = a.master[0];
+        p.w1 = p.wo1 = a.master[1];
+        p.m0 = p.mo0 = a.m[0];
+        p.m1 = p.mo1 = a.m[1];
+        p.v0 = p.vo0 = a.v[0];
+        p.v1 = p.vo1 = a.v[1];
+        p.par0 = static_cast<uint16_t *>(a.params[0]);
+        p.par1 = static_cast<uint16_t *>(a.params[1]);
+    }
+    p.stage = a.stage;
+    p.partials = a.partials;
+    const int ranks = a.rank < 0 ? world : 1;
+    *ranks_out = ranks;
+    return dispatch<MAXW>(p, a.dtype, mode, ranks, stream, gx);
+}
+
+int run(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ranks)
+{
+    if (a.lay->world <= 64)
+        return run_pass<64>(a, mode, stream, gx, ranks);
+    return run_pass<ZERO_MAX_WORLD>(a, mode, stream, gx, ranks);
+}
+
+int check_grads(const void *const *grads, int grads_are_slices, zero_dtype dtype,
+                const zero_layout *lay, int rank)
+{
+    int rc = check_layout(lay);
+    if (rc)
+        return rc;
+    if (!grads || (dtype != ZERO_F16 && dtype != ZERO_BF16) || rank < -1 || rank >= lay->world ||
+        (grads_are_slices && rank < 0))
+        return ZERO_EINVAL;
+    for (int q = 0; q < lay->world; ++q) {
+        if (!grads[q] && lay->padded_numel)
+            return ZERO_EINVAL;
+        if (!aligned16(grads[q]))
+            return ZERO_EALIGN;
+    }
+    return ZERO_OK;
+}
+
+}  // namespace zs
+
+using namespace zs;
+
+extern "C" int zero_reduce_scatter_sum(const void *const *grads, int grads_are_slices,
+                                       zero_dtype dtype, const zero_layout *layout, int rank,
+                                       float *g_out, zero_stream_t stream)
+{
+    int rc = check_grads(grads, grads_are_slices, dtype, layout, rank);
+    if (rc)
+        return rc;
+    if (!g_out)
+        return ZERO_EINVAL;
+    if (!aligned16(g_out))
+        return ZERO_EALIGN;
+    if (layout->padded_numel == 0)
+        return ZERO_OK;
+    PassArgs a{grads, grads_are_slices, dtype, layout, rank, nullptr, nullptr,
+               nullptr, nullptr, nullptr, nullptr, g_out, nullptr};
+    int gx, ranks;
+    return run(a, M_RS, stream, &gx, &ranks);
+}
+
+extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, zero_dtype dtype,
+                               const zero_layout *layout, int rank, float *const master[2],
+                               float *const m[2], float *const v[2], void *const params[2],
+                               float *g_stage, const zero_adam_cfg *cfg,
+                               zero_step_state *state_dev, void *ws, size_t ws_bytes,
+                               zero_stream_t stream)
+{
+    int rc = check_grads(grads, grads_are_slices, dtype, layout, rank);
+    if (rc)
+        return rc;
+    if ((rc = check_cfg(cfg)))
+        return rc;
+    if (!master || !m || !v || !params || !state_dev || !ws)
+        return ZERO_EINVAL;
+    const bool clip = cfg->max_grad_norm > 0.0;
+    for (int s = 0; s < 2; ++s) {
+        if (!master[s] || !m[s] || !v[s] || !params[s])
+            return ZERO_EINVAL;
+        if (!aligned16(master[s]) || !aligned16(m[s]) || !aligned16(v[s]) || !aligned16(params[s]))
+            return ZERO_EALIGN;
+    }
+    if (!clip && (master[0] == master[1] || m[0] == m[1] || v[0] == v[1] ||
+                  params[0] == params[1]))
+        return ZERO_EINVAL;  // a one-pass step needs distinct slots to be able to skip
+    if (g_stage && !clip)
+        return ZERO_EINVAL;
+    if ((g_stage && !aligned16(g_stage)) || !aligned16(ws) ||
+        (reinterpret_cast<uintptr_t>(state_dev) & 7u))
+        return ZERO_EALIGN;
+    if (ws_bytes < zero_workspace_bytes(layout->world))
+        return ZERO_ESPACE;
+
+    double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
+    PassArgs a{grads, grads_are_slices, dtype, layout, rank, cfg, state_dev,
+               master, m, v, params, g_stage, partials};
+    int gx = 1, ranks = 1;
+    if (layout->padded_numel > 0) {
+        if (!clip) {
+            if ((rc = run(a, M_FUSED, stream, &gx, &ranks)))
+                return rc;
+        } else {
+            if ((rc = run(a, M_PASS1, stream, &gx, &ranks)))
+                return rc;
+            if ((rc = launch_norm_finalize(partials, gx, ranks, cfg->max_grad_norm, state_dev,
+                                           nullptr, stream)))
+                return rc;
+            if ((rc = run(a, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE, stream, &gx, &ranks)))
+                return rc;
+        }
+    }
+    return launch_finalize(cfg, state_dev, 1, stream);
+}
