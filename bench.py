@@ -1,0 +1,413 @@
+"""Benchmark of the fused partitioned mixed-precision ZeRO Adam step on GB300.
+
+Default workload: the 1.5B-parameter flat vector over N_d = 16 simulated
+data-parallel ranks (fp16 gradients scaled by 2^12, dynamic loss scale, Adam
+without weight decay, +Inf injected every 50th step so those steps are
+skipped).  A step is one call of zero_step_fused: the reduce-scatter sum of
+the 16 gradient buffers, unscale, overflow check, Adam on the fp32 master
+weights and moments, and the fp16 cast into the flat parameter buffer.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+With --gpus N > 1 (under torchrun) every GPU runs its own replica of the
+workload (the simulated group does not span GPUs): weak scaling, no
+collective on the data path.  --impl reference times the CPU oracle on the
+host cores instead (rank 0 only).
+
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused ZeRO Adam step: G params updated/s and achieved HBM GB/s vs GB300 peak"
+UNIT = "Gparams/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes_per_elem(world: int, clip: bool, staged: bool) -> int:
+    """Bytes an ideal step moves per padded element: read the N_d half
+    gradients, read and write fp32 master/m/v, write the half parameter.
+    A clipped step needs a second pass: +8 (stage written and read) or
+    +2 N_d (gradients read again)."""
+    b = 2 * world + 24 + 2
+    if clip:
+        b += 8 if staged else 2 * world
+    return b
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "zero_partitioned_mixed_step_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per launch of the fused kernel from the committed ncu
+    summary, valid only while the kernel sources are unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload \
+                    and parts[1] == want:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        rows = [r.split(", ") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, power = [], [], []
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                power.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip() == "Active":
+                    reasons.add(name)
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] if power else sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- inputs
+
+def lib_cfg(wl):
+    import zero_partitioned_mixed_step_gb300 as zs
+    return zs.adam_cfg(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                       weight_decay=wl.weight_decay, adamw=wl.adamw,
+                       max_grad_norm=wl.max_grad_norm, dynamic_scale=wl.dynamic_scale)
+
+
+def make_group(wl, device):
+    """Device buffers of the workload, filled by the seeded GPU generator:
+    master ~ N(0, 0.02) by flat index, m = v = 0, params = RNE(master), and
+    every rank's step-1 gradient ~ N(0, 1e-3) x loss scale, zero in padding."""
+    import torch
+    import synth
+    import zero_partitioned_mixed_step_gb300 as zs
+
+    rank = -1 if wl.rank is None else wl.rank
+    z = zs.ZeroStep(wl.numels, wl.world, wl.dtype, lib_cfg(wl), loss_scale=wl.loss_scale,
+                    rank=rank, bucket_numel=wl.bucket, grads_are_slices=wl.grads_are_slices,
+                    device=device)
+    L = z.layout
+    gaps = synth.gaps(z.offsets, wl.numels, L.padded_numel)
+    segs = [(0, L.padded_numel)] if rank < 0 else z.segments(rank)
+
+    def fill_by_flat(out, fill):
+        pos = 0
+        for fs, ln in segs:
+            fill(out[pos:pos + ln], fs)
+            for a, b in gaps:  # zero the padding that falls inside this range
+                lo, hi = max(a, fs), min(b, fs + ln)
+                if lo < hi:
+                    out[pos + lo - fs:pos + hi - fs].zero_()
+            pos += ln
+
+    fill_by_flat(z.master[0], lambda o, fs: synth.gpu_fill_f32(wl.master_key(), fs, o,
+                                                               wl.master_sigma))
+    if rank < 0:
+        synth.gpu_round_half(z.master[0], z.params[0], wl.dtype)
+    hdt = zs.torch_dtype(wl.dtype)
+    grads = []
+    sigma = wl.grad_sigma * wl.loss_scale
+    for q in range(wl.world):
+        g = torch.empty(z.grad_numel(), dtype=hdt, device=device)
+        if wl.grads_are_slices:
+            fill_by_flat(g, lambda o, fs, q=q: synth.gpu_fill_half(wl.grad_key(1, q), fs, o,
+                                                                   sigma, wl.dtype))
+        else:
+            synth.gpu_fill_half(wl.grad_key(1, q), 0, g, sigma, wl.dtype)
+            for a, b in gaps:
+                g[a:b].zero_()
+        grads.append(g)
+    torch.cuda.synchronize()
+    return z, grads
+
+
+# --------------------------------------------------------------------------- CPU legs
+
+def oracle_sample_rate(wl, target_s: float = 12.0, sample_elems: int = 1 << 22):
+    """Time the CPU oracle (OpenMP build, all host cores) on a bounded sample
+    of the workload: the first ``sample_elems`` owned elements of one rank,
+    with all N_d gradient buffers, stepped repeatedly for ~target_s seconds.
+    Returns (params/s, threads, description)."""
+    import numpy as np
+    import oracle
+    import synth
+
+    n = sample_elems
+    lay = oracle.layout((n * wl.world,), wl.world)  # a flat sample with the same N_d
+    grads = [synth.fill_half(wl.grad_key(1, q), 0, lay.padded, wl.grad_sigma * wl.loss_scale,
+                             wl.dtype) for q in range(wl.world)]
+    cfg = oracle.AdamCfg(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                         weight_decay=wl.weight_decay, adamw=wl.adamw,
+                         max_grad_norm=wl.max_grad_norm, dynamic_scale=wl.dynamic_scale)
+    st = oracle.State(loss_scale=wl.loss_scale)
+    w = synth.fill_f32(wl.master_key(), 0, lay.owned, wl.master_sigma)
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    half = np.zeros(lay.padded, np.uint16)
+    oracle.step(grads, wl.dtype, lay, cfg, st, w, m, v, half, rank=0, openmp=True)  # warm
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.step(grads, wl.dtype, lay, cfg, st, w, m, v, half, rank=0, openmp=True)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"{steps} oracle steps of one rank's first {n} elements with all {wl.world} "
+            f"gradient buffers ({wl.world * n * 2 / 1e6:.0f} MB of gradients per step)")
+    return n * steps / el, threads, desc
+
+
+def run_reference(args, wl):
+    """--impl reference: the CPU oracle on the host cores, same metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rate, threads, desc = oracle_sample_rate(wl, target_s=max(6.0, 1.5 * args.steps))
+    value = rate / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wl.numel / rate * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "psi": wl.numel, "world": wl.world},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- GPU leg
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    import zero_partitioned_mixed_step_gb300 as zs
+
+    world_size = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    distributed = world_size > 1
+    if distributed:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    z, grads = make_group(wl, device)
+    L = z.layout
+    inf_bits = 0x7C00 if wl.dtype == zs.F16 else 0x7F80
+    stream = torch.cuda.current_stream()
+
+    # Overflow injection (every 50th step of the workload): one element of
+    # one rank's gradient is set to +Inf before the step and restored after.
+    def injections(step):
+        return [(q, i) for q, i in wl.injections(step)
+                if (not wl.grads_are_slices) or i < z.grad_numel()]
+
+    saved = {}
+
+    def before(step):
+        for q, i in injections(step):
+            saved[(q, i)] = grads[q][i:i + 1].clone()
+            grads[q][i:i + 1].view(torch.int16).fill_(inf_bits - 65536 if inf_bits > 32767 else inf_bits)
+
+    def after(step):
+        for q, i in injections(step):
+            grads[q][i:i + 1].copy_(saved.pop((q, i)))
+
+    for s in range(1, args.warmup + 1):
+        z.step(grads, stream)
+    torch.cuda.synchronize()
+
+    nsteps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(nsteps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if distributed:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for s in range(1, nsteps + 1):
+            before(s)
+            ev[s - 1][0].record(stream)
+            z.step(grads, stream)
+            ev[s - 1][1].record(stream)
+            after(s)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if distributed:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    if distributed:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st = z.read_state()
+
+    # end to end: the same step through the public API from pinned host buffers
+    e2e = run_e2e(z, grads, wl, args)
+
+    if rank != 0:
+        if distributed:
+            dist.destroy_process_group()
+        return
+    clip = wl.max_grad_norm > 0
+    bpe = algorithmic_bytes_per_elem(wl.world, clip, z.g_stage is not None)
+    n_elems = L.padded_numel if wl.rank is None else L.owned_numel
+    params_per_step = wl.numel if wl.rank is None else min(L.owned_numel, wl.numel)
+    value = params_per_step * nsteps * world_size / (total_ms / 1e3) / 1e9
+    kernel_ms = statistics.mean(step_ms)
+    achieved = n_elems * bpe / (kernel_ms / 1e3) / 1e9
+    peaks, kind = measured_peaks()
+    peak = peaks["hbm_gbs"]
+    traffic = recorded_traffic(wl.name)
+    rate, threads, desc = oracle_sample_rate(wl)
+    launches_per_step = 4 if clip else 2
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world_size,
+        "steps": nsteps, "warmup": args.warmup, "ms_per_step": total_ms / nsteps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "psi": wl.numel, "padded": L.padded_numel,
+                   "world": wl.world, "grad_dtype": "f16" if wl.dtype == zs.F16 else "bf16",
+                   "rank_view": wl.rank, "bucket": wl.bucket, "clip": clip,
+                   "bytes_per_elem": bpe, "replicas": world_size,
+                   "l2": "no flush: each step streams %.1f GB (> 129 MB L2)" % (n_elems * bpe / 1e9),
+                   "skipped_steps": st.skipped},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": f"{kind} hbm_gbs", "kernel": "step_kernel (fused, one pass)"
+                     if not clip else "step_kernel (two passes)",
+                     "kernel_ms": kernel_ms, "bytes_per_launch": n_elems * bpe},
+        "cpu_baseline": {"value": rate / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * nsteps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line))
+    if distributed:
+        dist.destroy_process_group()
+
+
+def run_e2e(z, grads, wl, args, steps: int = 3):
+    """Host -> device copies of every rank's gradient from pinned memory, the
+    step, and the device -> host read of the step state, all timed."""
+    import torch
+    try:
+        host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in grads]
+    except RuntimeError as e:  # not enough pinnable host memory
+        return {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "unavailable": f"pinned host buffers: {str(e).splitlines()[0]}"}
+    for h, g in zip(host, grads):
+        h.copy_(g)
+    stream = torch.cuda.current_stream()
+    z.step_from_host(host, grads, stream)  # warm-up
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        z.step_from_host(host, grads, stream)
+    el = time.perf_counter() - t0
+    h2d = sum(g.numel() * g.element_size() for g in grads)
+    params = wl.numel if wl.rank is None else min(z.layout.owned_numel, wl.numel)
+    del host
+    return {"value": params * steps / el / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": 64, "steps": steps}
+
+
+def main():
+    from synth.workloads import BY_NAME, CFG3
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=CFG3.name, choices=sorted(BY_NAME))
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -391,19 +391,21 @@ def step(grads: Sequence[np.ndarray], dtype: int, lay: Layout, cfg: AdamCfg, st:
 
 
 def scan_scalars(grad_chunks, dtype: int, lay: Layout, inv_scale: float, want_sumsq: bool,
-                 openmp: bool = False) -> Tuple[bool, float]:
+                 openmp: bool = False, ranks: Optional[Sequence[int]] = None,
+                 chunk: int = 1 << 24) -> Tuple[bool, float]:
     """The step's global scalars (overflow flag, sum of squares) for gradients
     too large to hold at once.  ``grad_chunks(r, flat_start, n)`` returns the
     world gradient arrays for flat elements [flat_start, flat_start + n);
     chunks are taken in each rank's element order, so the sum of squares is
-    the same sequential sum ``step`` forms."""
+    the same sequential sum ``step`` forms.  ``ranks``: the simulated ranks
+    (all by default)."""
     flag = False
     total = 0.0
-    for r in range(lay.world):
+    for r in (range(lay.world) if ranks is None else ranks):
         acc = 0.0
         for fs, ln in lay.segments[r]:
-            for chunk_start in range(fs, fs + ln, 1 << 24):
-                n = min(1 << 24, fs + ln - chunk_start)
+            for chunk_start in range(fs, fs + ln, chunk):
+                n = min(chunk, fs + ln - chunk_start)
                 gs = grad_chunks(r, chunk_start, n)
                 g = reduce_sum(gs, dtype, 0, n, openmp)
                 unscale(g, inv_scale, openmp)

@@ -129,4 +129,10 @@ CFG5 = Workload("8B-decoder-nd8-bf16-bucket25M-clip", decoder_8b_numels(), 8, BF
                 False, max_grad_norm=1.0, steps=10, seed=1005, bucket=25_000_000, **ADAMW)
 
 ALL = (CFG1, CFG2, CFG3, CFG4, CFG5)
-BY_NAME = {w.name: w for w in ALL}
+
+# A smaller case of the 1.5B workload for detailed profiles: 64M elements
+# with the same 16 ranks; one launch still streams ~3.7 GB (far above L2)
+# while the buffers hold ~4 GB of device memory.
+PROFILE_CFG3 = CFG3.replace(name="flat-64M-nd16-fp16-dynamic", numels=(64_000_000,))
+
+BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3,)}

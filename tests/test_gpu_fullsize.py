@@ -1,0 +1,266 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times (ZeroStep.step -> zero_step_fused).
+
+The gradients are produced on the GPU by the seeded generator (bit-identical
+to the CPU generator, see test_gpu_parity.test_generators_agree) and
+regenerated every step with the current loss scale.  The oracle forms each
+step's global scalars (overflow flag, sum of squares) from a full scan of
+those gradients, streamed to the host chunk by chunk in each rank's element
+order, and then steps windows of elements on its own (the update is
+element-wise once the scalars are known); the CUDA results are compared on
+those windows: partition, bucket and tensor boundaries, the padded tail and
+random interior elements.  The GPT-2-sized workload is compared in full."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.workloads import CFG2, CFG3, CFG4, CFG5
+import zero_partitioned_mixed_step_gb300 as zs
+from zs_harness import (INF_BITS, SUMSQ_RTOL, assert_close, assert_half_close, half_bits,
+                        lib_cfg, oracle_cfg)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+WIN = 4096
+
+
+class GpuGroup:
+    """A workload's buffers on the GPU, filled by the seeded generator."""
+
+    def __init__(self, wl, stage=None):
+        self.wl = wl
+        self.lay = oracle.layout(wl.numels, wl.world, wl.align, wl.bucket)
+        rank = -1 if wl.rank is None else wl.rank
+        self.z = zs.ZeroStep(wl.numels, wl.world, wl.dtype, lib_cfg(wl), loss_scale=wl.loss_scale,
+                             rank=rank, bucket_numel=wl.bucket, align_elems=wl.align,
+                             grads_are_slices=wl.grads_are_slices, stage_grad=stage)
+        self.gaps = synth.gaps(self.lay.offsets, wl.numels, self.lay.padded)
+        self.segs = ([(0, self.lay.padded)] if wl.rank is None else
+                     list(self.lay.segments[wl.rank]))
+        self._fill_by_flat(self.z.master[0],
+                           lambda o, fs: synth.gpu_fill_f32(wl.master_key(), fs, o,
+                                                            wl.master_sigma))
+        if wl.rank is None:
+            synth.gpu_round_half(self.z.master[0], self.z.params[0], wl.dtype)
+        hdt = zs.torch_dtype(wl.dtype)
+        n = self.lay.owned if wl.grads_are_slices else self.lay.padded
+        self.grads = [torch.empty(n, dtype=hdt, device="cuda") for _ in range(wl.world)]
+        self.host = [torch.empty(1 << 24, dtype=torch.int16, pin_memory=True)
+                     for _ in range(wl.world)]
+
+    def _fill_by_flat(self, out, fill):
+        pos = 0
+        for fs, ln in self.segs:
+            fill(out[pos:pos + ln], fs)
+            for a, b in self.gaps:
+                lo, hi = max(a, fs), min(b, fs + ln)
+                if lo < hi:
+                    out[pos + lo - fs:pos + hi - fs].zero_()
+            pos += ln
+
+    def local_of(self, flat):
+        """Index of flat element `flat` in a rank-local buffer (None if not owned)."""
+        pos = 0
+        for fs, ln in self.segs:
+            if fs <= flat < fs + ln:
+                return pos + flat - fs
+            pos += ln
+        return None
+
+    def regen(self, step, loss_scale):
+        wl = self.wl
+        sigma = wl.grad_sigma * loss_scale
+        for q, g in enumerate(self.grads):
+            if wl.grads_are_slices:
+                self._fill_by_flat(g, lambda o, fs: synth.gpu_fill_half(
+                    wl.grad_key(step, q), fs, o, sigma, wl.dtype))
+            else:
+                synth.gpu_fill_half(wl.grad_key(step, q), 0, g, sigma, wl.dtype)
+                for a, b in self.gaps:
+                    g[a:b].zero_()
+        for q, i in wl.injections(step):
+            j = self.local_of(i) if wl.grads_are_slices else i
+            if j is not None:
+                self.grads[q][j:j + 1].view(torch.int16).fill_(INF_BITS[wl.dtype])
+
+    def chunk(self, r, flat_start, n):
+        """The world gradient arrays for flat elements [flat_start, +n)."""
+        j = self.local_of(flat_start) if self.wl.grads_are_slices else flat_start
+        out = []
+        for g, h in zip(self.grads, self.host):
+            h[:n].copy_(g[j:j + n].view(torch.int16), non_blocking=True)
+        torch.cuda.synchronize()
+        for h in self.host:
+            out.append(h[:n].numpy().view(np.uint16).copy())
+        return out
+
+
+def pick_windows(lay, wl, seed=0):
+    """(rank, local start, length) windows, each inside one owned segment."""
+    rnd = np.random.default_rng(seed)
+    ranks = [wl.rank] if wl.rank is not None else sorted({0, 1, wl.world // 2, wl.world - 1})
+    wins = set()
+    for r in ranks:
+        local = 0
+        segs = lay.segments[r]
+        for si, (fs, ln) in enumerate(segs):
+            n = min(WIN, ln)
+            if si in (0, 1, len(segs) - 1):
+                wins.add((r, local, n))
+                wins.add((r, local + ln - n, n))
+            local += ln
+        for _ in range(3):
+            k = int(rnd.integers(0, max(1, lay.owned - WIN))) // 8 * 8
+            wins.add((r, k, min(WIN, lay.owned - k)))
+    # tensor starts and ends that fall in a simulated rank
+    for o, nt in list(zip(lay.offsets, lay.numels))[:: max(1, len(lay.numels) // 6)]:
+        for flat in (o, o + nt - 1):
+            for r in ranks:
+                local = 0
+                for fs, ln in lay.segments[r]:
+                    if fs <= flat < fs + ln:
+                        k = max(local, local + (flat - fs) - WIN // 2) // 8 * 8
+                        k = max(k, local)
+                        wins.add((r, k, min(WIN, local + ln - k)))
+                    local += ln
+    return sorted(wins)
+
+
+def window_mask(lay, f0, n):
+    """True where flat elements f0 .. f0+n-1 belong to a tensor (not padding)."""
+    mask = np.zeros(n, bool)
+    for o, nt in zip(lay.offsets, lay.numels):
+        lo, hi = max(o, f0), min(o + nt, f0 + n)
+        if lo < hi:
+            mask[lo - f0:hi - f0] = True
+    return mask
+
+
+def flat_of_local(lay, r, k, n):
+    """Flat indices of rank r's local elements k .. k+n-1 (one segment)."""
+    local = 0
+    for fs, ln in lay.segments[r]:
+        if local <= k < local + ln:
+            assert k + n <= local + ln
+            return fs + (k - local)
+        local += ln
+    raise AssertionError("window outside the rank")
+
+
+def run_windowed(wl, steps, stage=None):
+    grp = GpuGroup(wl, stage)
+    lay, z = grp.lay, grp.z
+    cfg = oracle_cfg(wl)
+    st = oracle.State(loss_scale=wl.loss_scale)
+    wins = pick_windows(lay, wl)
+    master0 = {}
+    state = {}
+    for (r, k, n) in wins:
+        f0 = flat_of_local(lay, r, k, n)
+        w = synth.fill_f32(wl.master_key(), f0, n, wl.master_sigma)
+        w[~window_mask(lay, f0, n)] = 0
+        master0[(r, k, n)] = f0
+        state[(r, k, n)] = [w, np.zeros(n, np.float32), np.zeros(n, np.float32),
+                            synth.round_half(w, wl.dtype)]
+    ranks = None if wl.rank is None else [wl.rank]
+    for s in range(1, steps + 1):
+        S = st.loss_scale
+        grp.regen(s, S)
+        z.step(grp.grads)
+        flag, sumsq = oracle.scan_scalars(grp.chunk, wl.dtype, lay, oracle.f32(1.0 / S),
+                                          cfg.max_grad_norm > 0, openmp=True, ranks=ranks)
+        for key, (w, m, v, h) in state.items():
+            r, k, n = key
+            f0 = master0[key]
+            mask = window_mask(lay, f0, n)
+            gw = []
+            for q in range(wl.world):
+                g = synth.fill_half(wl.grad_key(s, q), f0, n, wl.grad_sigma * S, wl.dtype)
+                g[~mask] = 0
+                for qq, i in wl.injections(s):
+                    if qq == q and f0 <= i < f0 + n:
+                        g[i - f0] = INF_BITS[wl.dtype]
+                gw.append(g)
+            out = oracle.window_step(gw, wl.dtype, cfg, st, flag, sumsq, w, m, v)
+            if out is not None:
+                h[:] = out
+        if flag:
+            oracle.skip(cfg, st)
+        else:
+            if cfg.max_grad_norm > 0:
+                st.sumsq = sumsq
+                st.coef = oracle.clip_coef(sumsq, cfg.max_grad_norm)
+            oracle.commit(cfg, st)
+        torch.cuda.synchronize()
+        zst = z.read_state()
+        assert (zst.overflow, zst.t, zst.skipped, zst.loss_scale) == \
+            (st.overflow, st.t, st.skipped, st.loss_scale), s
+        if cfg.max_grad_norm > 0 and not flag:
+            assert abs(zst.sumsq - sumsq) <= SUMSQ_RTOL * sumsq
+            assert abs(zst.clip_coef - st.coef) <= 2.0 ** -23 * st.coef
+        w_d, m_d, v_d, p_d = z.current()
+        for key, (w, m, v, h) in state.items():
+            r, k, n = key
+            f0 = master0[key]
+            si = f0 if wl.rank is None else k
+            assert_close(f"master{key}", w_d[si:si + n].cpu().numpy(), w)
+            assert_close(f"m{key}", m_d[si:si + n].cpu().numpy(), m)
+            assert_close(f"v{key}", v_d[si:si + n].cpu().numpy(), v)
+            assert_half_close(f"params{key}", half_bits(p_d[f0:f0 + n]), h)
+    return st
+
+
+def test_fullsize_1p5B_nd16_dynamic():
+    """1.5B flat, 16 ranks, fp16 x 2^12, dynamic loss scale; +Inf in steps 2
+    and 4 (the workload injects every 50th step; here every 2nd so the short
+    run skips twice)."""
+    st = run_windowed(CFG3.replace(inject_every=2), steps=5)
+    assert st.skipped == 2 and st.t == 3 and st.loss_scale == 1024.0
+
+
+def test_fullsize_7p5B_rank0_nd64():
+    """Rank 0 of 64 over a 7.5B vector: 64 slice buffers of 117,187,520."""
+    st = run_windowed(CFG4.replace(inject_at=((2, 17, 1_000_000),)), steps=3)
+    assert st.skipped == 1 and st.t == 2
+
+
+def test_fullsize_8B_buckets_clip():
+    """The 8B decoder list over 8 ranks in 25M-element buckets with the
+    global-norm clip (two passes, gradient staged in fp32)."""
+    free, _ = torch.cuda.mem_get_info()
+    need = 8 * 8_030_261_248 * 2 + 8_030_261_248 * (12 + 2 + 4) + (2 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+    st = run_windowed(CFG5, steps=2, stage=True)
+    assert st.t == 2
+
+
+def test_fullsize_gpt2_nd8_clip_every_element():
+    """GPT-2-small list over 8 ranks with the clip: every element compared."""
+    wl = CFG2.replace(steps=3)
+    grp = GpuGroup(wl)
+    lay, z = grp.lay, grp.z
+    cfg = oracle_cfg(wl)
+    st = oracle.State()
+    w = z.master[0].cpu().numpy().copy()
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    half = half_bits(z.params[0]).copy()
+    for s in range(1, wl.steps + 1):
+        grp.regen(s, st.loss_scale)
+        z.step(grp.grads)
+        grads = [half_bits(g) for g in grp.grads]
+        oracle.step(grads, wl.dtype, lay, cfg, st, w, m, v, half, openmp=True)
+        torch.cuda.synchronize()
+        zst = z.read_state()
+        assert (zst.overflow, zst.t) == (st.overflow, st.t)
+        assert abs(zst.sumsq - st.sumsq) <= SUMSQ_RTOL * st.sumsq
+        assert abs(zst.clip_coef - st.coef) <= 2.0 ** -23 * st.coef
+        w_d, m_d, v_d, p_d = z.current()
+        assert_close("master", w_d.cpu().numpy(), w)
+        assert_close("m", m_d.cpu().numpy(), m)
+        assert_close("v", v_d.cpu().numpy(), v)
+        assert_half_close("params", half_bits(p_d), half)
+    assert st.coef < 1.0  # the clip was active

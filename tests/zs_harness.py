@@ -25,9 +25,11 @@ def oracle_cfg(wl) -> oracle.AdamCfg:
 
 
 def lib_cfg(wl, **kw):
-    return zs.adam_cfg(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
-                       weight_decay=wl.weight_decay, adamw=wl.adamw,
-                       max_grad_norm=wl.max_grad_norm, dynamic_scale=wl.dynamic_scale, **kw)
+    args = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                weight_decay=wl.weight_decay, adamw=wl.adamw, max_grad_norm=wl.max_grad_norm,
+                dynamic_scale=wl.dynamic_scale)
+    args.update(kw)
+    return zs.adam_cfg(**args)
 
 
 def tensor_mask(lay: oracle.Layout) -> np.ndarray:

@@ -204,6 +204,19 @@ class ZeroStep:
         self.state = new_state(loss_scale, device)
         self.ws = torch.empty(zero_workspace_bytes(world), dtype=torch.uint8, device=device)
 
+    def segments(self, r: int) -> List[Tuple[int, int]]:
+        """(flat start, length) of the ranges rank r owns, in r's element order."""
+        L = self.layout
+        if L.padded_numel == 0:
+            return []
+        if L.bucket_numel == 0:
+            return [(r * L.owned_numel, L.owned_numel)]
+        segs = [(b * L.bucket_numel + r * L.slice_numel, L.slice_numel)
+                for b in range(L.num_buckets - 1)]
+        segs.append(((L.num_buckets - 1) * L.bucket_numel + r * L.last_slice_numel,
+                     L.last_slice_numel))
+        return segs
+
     def grad_numel(self) -> int:
         """Elements of each rank's gradient buffer."""
         return self.layout.owned_numel if self.grads_are_slices else self.layout.padded_numel
@@ -218,14 +231,15 @@ class ZeroStep:
         """End to end: copy each rank's gradient from (pinned) host memory,
         run the step and read the step state back to the host."""
         s = stream if stream is not None else torch.cuda.current_stream()
+        if getattr(self, "_state_host", None) is None:
+            self._state_host = torch.empty(64, dtype=torch.uint8, pin_memory=True)
         with torch.cuda.stream(s):
             for h, d in zip(host_grads, device_grads):
                 d.copy_(h, non_blocking=True)
             self.step(device_grads, s)
-            out = torch.empty(64, dtype=torch.uint8, pin_memory=True)
-            out.copy_(self.state, non_blocking=True)
+            self._state_host.copy_(self.state, non_blocking=True)
         s.synchronize()
-        return StepState.from_buffer_copy(bytes(out.numpy().tobytes()))
+        return StepState.from_buffer_copy(bytes(self._state_host.numpy().tobytes()))
 
     def read_state(self) -> StepState:
         return read_state(self.state)

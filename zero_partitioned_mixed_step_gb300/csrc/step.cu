@@ -304,14 +304,15 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
     if (!master || !m || !v || !params || !state_dev || !ws)
         return ZERO_EINVAL;
     const bool clip = cfg->max_grad_norm > 0.0;
+    const bool empty = layout->padded_numel == 0;  // nothing to read or write
     for (int s = 0; s < 2; ++s) {
-        if (!master[s] || !m[s] || !v[s] || !params[s])
+        if (!empty && (!master[s] || !m[s] || !v[s] || !params[s]))
             return ZERO_EINVAL;
         if (!aligned16(master[s]) || !aligned16(m[s]) || !aligned16(v[s]) || !aligned16(params[s]))
             return ZERO_EALIGN;
     }
-    if (!clip && (master[0] == master[1] || m[0] == m[1] || v[0] == v[1] ||
-                  params[0] == params[1]))
+    if (!clip && !empty &&
+        (master[0] == master[1] || m[0] == m[1] || v[0] == v[1] || params[0] == params[1]))
         return ZERO_EINVAL;  // a one-pass step needs distinct slots to be able to skip
     if (g_stage && !clip)
         return ZERO_EINVAL;
