@@ -143,10 +143,16 @@ __device__ __forceinline__ void reduce_unit(const GradTable<MAXW> &t, int world,
 
 // ------------------------------------------------------------------ element mapping
 
-// Which elements a launch covers.  A launch has gridDim.y ranks; the CTA row
-// y processes rank rank0 + y, walking that rank's owned units k = 0, 1, ...
+// Which elements a launch covers.  A launch walks units u = 0 .. units - 1
+// with a grid stride over a one-dimensional grid.
+//  - every rank at once (all_ranks): the union of the partitions is the whole
+//    padded flat vector, so unit u is flat elements 8u .. 8u + 7 and the
+//    state buffers are flat too;
+//  - one rank r: unit u is r's u-th group of 8 owned elements; its flat
+//    position follows the partition (or bucket-slice) layout, and the state
+//    buffers hold r's elements in order.
 struct View {
-    int64_t owned_units;   // units each rank owns (owned_numel / 8)
+    int64_t units;         // units the launch covers
     int64_t part;          // owned_numel (flat stride between partitions, not bucketed)
     int64_t bucket;        // elements per bucket, 0 = not bucketed
     int64_t slice;         // a rank's elements in a full bucket
@@ -154,12 +160,13 @@ struct View {
     int64_t full_units;    // units in the full buckets: (num_buckets - 1) * slice_units
     int64_t last_base;     // flat start of the last bucket
     int64_t last_slice;    // a rank's elements in the last bucket
-    int32_t rank0;
-    int32_t all_ranks;     // 1: state buffers are flat (state index = flat index)
+    int32_t rank;          // the simulated rank when !all_ranks
+    int32_t all_ranks;
     int32_t grads_are_slices;
     int32_t world;
 };
 
+// Flat element index of rank r's owned unit k (one-rank view).
 __device__ __forceinline__ int64_t flat_of(const View &v, int r, int64_t k)
 {
     const int64_t e = k * kUnit;
@@ -174,6 +181,19 @@ __device__ __forceinline__ int64_t flat_of(const View &v, int r, int64_t k)
         return b * v.bucket + (int64_t)r * v.slice + (e - b * v.slice);
     }
     return v.last_base + (int64_t)r * v.last_slice + (e - v.full_units * kUnit);
+}
+
+// Flat index f, state index si and gradient index gi of unit u.
+__device__ __forceinline__ void locate(const View &v, int64_t u, int64_t &f, int64_t &si,
+                                       int64_t &gi)
+{
+    if (v.all_ranks) {
+        f = si = gi = u * kUnit;
+    } else {
+        f = flat_of(v, v.rank, u);
+        si = u * kUnit;
+        gi = v.grads_are_slices ? si : f;
+    }
 }
 
 // ------------------------------------------------------------------ per-step scalars

@@ -3,8 +3,9 @@
 //
 // One kernel template covers the passes over the data.  Each thread handles
 // 8-element units (16-byte loads of each rank's half gradient, 32-byte loads
-// and stores of each fp32 state array), CTA row y walks rank rank0 + y's owned
-// units with a grid stride, and the grid is sized to fill every SM once.
+// and stores of each fp32 state array) with a grid stride; the grid is one
+// wave: exactly as many CTAs as the SMs hold at once (every CTA does the same
+// share of the work, so a second, partial wave would only add a tail).
 //   FUSED      (a2)-(a7) in one pass: reduce, unscale, flag, Adam from slot
 //              cur into slot 1 - cur, cast into the parameter buffer.
 //   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, per-CTA
@@ -53,7 +54,6 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
     const View &vw = p.view;
-    const int r = vw.rank0 + (int)blockIdx.y;
     const float *w_src = cur ? p.w1 : p.w0;
     const float *m_src = cur ? p.m1 : p.m0;
     const float *v_src = cur ? p.v1 : p.v0;
@@ -65,14 +65,13 @@ __global__ void __launch_bounds__(kThreads)
     bool bad = false;
     SumSq ss;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < vw.owned_units; k += stride) {
-        const int64_t f = flat_of(vw, r, k);
-        const int64_t si = vw.all_ranks ? f : k * kUnit;
+    for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < vw.units; u += stride) {
+        int64_t f, si, gi;
+        locate(vw, u, f, si, gi);
         float g[8];
         if constexpr (MODE == M_PASS2_STAGED) {
             load8(p.stage + si, g);
         } else {
-            const int64_t gi = vw.grads_are_slices ? k * kUnit : f;
             reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g);
             if constexpr (MODE == M_RS) {
                 store8(p.stage + si, g);
@@ -115,63 +114,58 @@ __global__ void __launch_bounds__(kThreads)
     if constexpr (MODE == M_PASS1) {
         const double tot = block_sum(ss.acc);
         if (threadIdx.x == 0)
-            p.partials[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = tot;
+            p.partials[blockIdx.x] = tot;
     }
 }
 
 // ------------------------------------------------------------------ launch
 
 template <int DT, int W, int MAXW, int MODE>
-int launch_one(const StepParams<MAXW> &p, int ranks, cudaStream_t stream, int *gx_out)
+int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
 {
     auto kern = step_kernel<DT, W, MAXW, MODE>;
     const int target = target_ctas(reinterpret_cast<const void *>(kern));
-    const int64_t want = (p.view.owned_units + kThreads - 1) / kThreads;
-    int64_t gx = (target + ranks - 1) / ranks;
-    if (want < gx)
-        gx = want;
-    if (gx < 1)
-        gx = 1;
+    const int64_t want = (p.view.units + kThreads - 1) / kThreads;
+    const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
     if (gx_out)
         *gx_out = (int)gx;
-    kern<<<dim3((unsigned)gx, (unsigned)ranks), kThreads, 0, stream>>>(p);
+    kern<<<(unsigned)gx, kThreads, 0, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
 
 template <int DT, int MAXW, int MODE>
-int dispatch_world(const StepParams<MAXW> &p, int ranks, cudaStream_t stream, int *gx)
+int dispatch_world(const StepParams<MAXW> &p, cudaStream_t stream, int *gx)
 {
     if constexpr (MODE == M_PASS2_STAGED) {
-        return launch_one<DT, 0, MAXW, MODE>(p, ranks, stream, gx);
+        return launch_one<DT, 0, MAXW, MODE>(p, stream, gx);
     } else if constexpr (MAXW == 64) {
         switch (p.view.world) {
-        case 2: return launch_one<DT, 2, MAXW, MODE>(p, ranks, stream, gx);
-        case 4: return launch_one<DT, 4, MAXW, MODE>(p, ranks, stream, gx);
-        case 8: return launch_one<DT, 8, MAXW, MODE>(p, ranks, stream, gx);
-        case 16: return launch_one<DT, 16, MAXW, MODE>(p, ranks, stream, gx);
-        case 32: return launch_one<DT, 32, MAXW, MODE>(p, ranks, stream, gx);
-        case 64: return launch_one<DT, 64, MAXW, MODE>(p, ranks, stream, gx);
-        default: return launch_one<DT, 0, MAXW, MODE>(p, ranks, stream, gx);
+        case 2: return launch_one<DT, 2, MAXW, MODE>(p, stream, gx);
+        case 4: return launch_one<DT, 4, MAXW, MODE>(p, stream, gx);
+        case 8: return launch_one<DT, 8, MAXW, MODE>(p, stream, gx);
+        case 16: return launch_one<DT, 16, MAXW, MODE>(p, stream, gx);
+        case 32: return launch_one<DT, 32, MAXW, MODE>(p, stream, gx);
+        case 64: return launch_one<DT, 64, MAXW, MODE>(p, stream, gx);
+        default: return launch_one<DT, 0, MAXW, MODE>(p, stream, gx);
         }
     } else {
-        return launch_one<DT, 0, MAXW, MODE>(p, ranks, stream, gx);
+        return launch_one<DT, 0, MAXW, MODE>(p, stream, gx);
     }
 }
 
 template <int MAXW>
-int dispatch(const StepParams<MAXW> &p, zero_dtype dt, int mode, int ranks, cudaStream_t s,
-             int *gx)
+int dispatch(const StepParams<MAXW> &p, zero_dtype dt, int mode, cudaStream_t s, int *gx)
 {
 #define ZS_MODES(DT)                                                      \
     switch (mode) {                                                       \
-    case M_FUSED: return dispatch_world<DT, MAXW, M_FUSED>(p, ranks, s, gx); \
-    case M_PASS1: return dispatch_world<DT, MAXW, M_PASS1>(p, ranks, s, gx); \
+    case M_FUSED: return dispatch_world<DT, MAXW, M_FUSED>(p, s, gx); \
+    case M_PASS1: return dispatch_world<DT, MAXW, M_PASS1>(p, s, gx); \
     case M_PASS2_RECOMPUTE:                                               \
-        return dispatch_world<DT, MAXW, M_PASS2_RECOMPUTE>(p, ranks, s, gx); \
+        return dispatch_world<DT, MAXW, M_PASS2_RECOMPUTE>(p, s, gx); \
     case M_PASS2_STAGED:                                                  \
-        return dispatch_world<DT, MAXW, M_PASS2_STAGED>(p, ranks, s, gx); \
-    default: return dispatch_world<DT, MAXW, M_RS>(p, ranks, s, gx);     \
+        return dispatch_world<DT, MAXW, M_PASS2_STAGED>(p, s, gx); \
+    default: return dispatch_world<DT, MAXW, M_RS>(p, s, gx);     \
     }
     if (dt == ZERO_F16) {
         ZS_MODES(ZERO_F16)
@@ -197,7 +191,7 @@ struct PassArgs {
 };
 
 template <int MAXW>
-int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ranks_out)
+int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
 {
     StepParams<MAXW> p{};
     const zero_layout &L = *a.lay;
@@ -206,7 +200,7 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ran
         for (int q = 0; q < world; ++q)
             p.grads.p[q] = static_cast<const uint16_t *>(a.grads[q]);
     View &v = p.view;
-    v.owned_units = L.owned_numel / kUnit;
+    v.units = (a.rank < 0 ? L.padded_numel : L.owned_numel) / kUnit;
     v.part = L.owned_numel;
     v.bucket = L.bucket_numel;
     v.slice = L.slice_numel;
@@ -214,7 +208,7 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ran
     v.full_units = L.bucket_numel ? (L.num_buckets - 1) * (L.slice_numel / kUnit) : 0;
     v.last_base = L.bucket_numel ? (L.num_buckets - 1) * L.bucket_numel : 0;
     v.last_slice = L.last_slice_numel;
-    v.rank0 = a.rank < 0 ? 0 : a.rank;
+    v.rank = a.rank < 0 ? 0 : a.rank;
     v.all_ranks = a.rank < 0;
     v.grads_are_slices = a.grads_are_slices;
     v.world = world;
@@ -236,16 +230,14 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ran
     }
     p.stage = a.stage;
     p.partials = a.partials;
-    const int ranks = a.rank < 0 ? world : 1;
-    *ranks_out = ranks;
-    return dispatch<MAXW>(p, a.dtype, mode, ranks, stream, gx);
+    return dispatch<MAXW>(p, a.dtype, mode, stream, gx);
 }
 
-int run(const PassArgs &a, int mode, cudaStream_t stream, int *gx, int *ranks)
+int run(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
 {
     if (a.lay->world <= 64)
-        return run_pass<64>(a, mode, stream, gx, ranks);
-    return run_pass<ZERO_MAX_WORLD>(a, mode, stream, gx, ranks);
+        return run_pass<64>(a, mode, stream, gx);
+    return run_pass<ZERO_MAX_WORLD>(a, mode, stream, gx);
 }
 
 int check_grads(const void *const *grads, int grads_are_slices, zero_dtype dtype,
@@ -285,8 +277,8 @@ extern "C" int zero_reduce_scatter_sum(const void *const *grads, int grads_are_s
         return ZERO_OK;
     PassArgs a{grads, grads_are_slices, dtype, layout, rank, nullptr, nullptr,
                nullptr, nullptr, nullptr, nullptr, g_out, nullptr};
-    int gx, ranks;
-    return run(a, M_RS, stream, &gx, &ranks);
+    int gx;
+    return run(a, M_RS, stream, &gx);
 }
 
 extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, zero_dtype dtype,
@@ -325,18 +317,18 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
     double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
     PassArgs a{grads, grads_are_slices, dtype, layout, rank, cfg, state_dev,
                master, m, v, params, g_stage, partials};
-    int gx = 1, ranks = 1;
+    int gx = 1;
     if (layout->padded_numel > 0) {
         if (!clip) {
-            if ((rc = run(a, M_FUSED, stream, &gx, &ranks)))
+            if ((rc = run(a, M_FUSED, stream, &gx)))
                 return rc;
         } else {
-            if ((rc = run(a, M_PASS1, stream, &gx, &ranks)))
+            if ((rc = run(a, M_PASS1, stream, &gx)))
                 return rc;
-            if ((rc = launch_norm_finalize(partials, gx, ranks, cfg->max_grad_norm, state_dev,
+            if ((rc = launch_norm_finalize(partials, gx, 1, cfg->max_grad_norm, state_dev,
                                            nullptr, stream)))
                 return rc;
-            if ((rc = run(a, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE, stream, &gx, &ranks)))
+            if ((rc = run(a, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE, stream, &gx)))
                 return rc;
         }
     }
