@@ -61,7 +61,9 @@
  *    code below.  A value <= ZERO_ECUDA_BASE is ZERO_ECUDA_BASE - cudaError_t
  *    of a failed launch.  Kernels never trap: numerical overflow is reported
  *    through zero_step_state, not as an error.
- *  - Vector buffers must be 16-byte aligned (ZERO_EALIGN otherwise).
+ *  - fp32 vector buffers (master, m, v, gradients in fp32, stages) must be
+ *    32-byte aligned and half-precision buffers 16-byte aligned (ZERO_EALIGN
+ *    otherwise): the kernels move 8 elements per access.
  */
 #ifndef ZEROSTEP_H
 #define ZEROSTEP_H
@@ -79,7 +81,7 @@ typedef struct CUstream_st *zero_stream_t; /* the same type as cudaStream_t */
 enum {
     ZERO_OK = 0,
     ZERO_EINVAL = -1,        /* null pointer, bad size, world, rank, dtype, config or layout */
-    ZERO_EALIGN = -2,        /* a buffer is not 16-byte aligned */
+    ZERO_EALIGN = -2,        /* a buffer is not aligned (32 bytes fp32, 16 bytes half) */
     ZERO_ESPACE = -3,        /* workspace smaller than zero_workspace_bytes() */
     ZERO_ECUDA_BASE = -1000  /* ZERO_ECUDA_BASE - cudaError_t */
 };
@@ -197,7 +199,8 @@ int zero_reduce_scatter_sum(const void *const *grads, int grads_are_slices, zero
 /*
  * Step (a4): *flag_dev |= 1 if any g[j] * inv_scale (j < n) is NaN or +-Inf;
  * otherwise *flag_dev is left as it is (clear it before the first call; pass
- * &state->found_inf to feed zero_adam_step).  g: device, n floats.
+ * &state->found_inf to feed zero_adam_step).  g: device, n floats, 16-byte
+ * aligned.
  * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "权重更新的触发条件".
  */
 int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *flag_dev,

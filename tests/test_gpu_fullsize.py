@@ -26,6 +26,18 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 WIN = 4096
 
 
+@pytest.fixture(autouse=True)
+def _release_device_memory():
+    """Each full-size workload needs most of the device: return the previous
+    test's cached blocks to the driver before and after."""
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
 class GpuGroup:
     """A workload's buffers on the GPU, filled by the seeded generator."""
 

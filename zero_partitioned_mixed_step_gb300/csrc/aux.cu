@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t n4 = n / 4;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < n4; k += stride) {
-        const float4 x = ld_state(g + 4 * k);
+        const float4 x = ld_state4(g + 4 * k);
         bad |= nonfinite(__fmul_rn(x.x, inv_s)) | nonfinite(__fmul_rn(x.y, inv_s)) |
                nonfinite(__fmul_rn(x.z, inv_s)) | nonfinite(__fmul_rn(x.w, inv_s));
     }
@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads)
     const Scalars s = sh;
     if (s.skip)
         return;
+    const uint64_t pol = evict_first_policy();
     const bool scale = s.clip && s.coef < 1.0f;
     const int64_t units = n / kUnit;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kThreads)
         store8(w + e, ww);
         store8(m + e, mm);
         store8(v + e, vv);
-        st_half8(out + e, pack_half8<DT>(ww));
+        st_half8(out + e, pack_half8<DT>(ww), pol);
     }
     if (blockIdx.x == 0 && threadIdx.x < (n % kUnit)) {
         const int64_t e = units * kUnit + threadIdx.x;
@@ -232,7 +233,7 @@ int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev
     if (n < 0 || !sumsq_dev || !ws || (n > 0 && !g) || !(inv_scale > 0.0f) ||
         !std::isfinite(inv_scale))
         return ZERO_EINVAL;
-    if (!aligned16(g) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(sumsq_dev) & 7u))
+    if (!aligned32(g) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(sumsq_dev) & 7u))
         return ZERO_EALIGN;
     if (ws_bytes < zero_workspace_bytes(1))
         return ZERO_ESPACE;
@@ -255,7 +256,7 @@ int zero_adam_step(const float *g, float *master, float *m, float *v, void *half
     if (n < 0 || !state_dev || (dtype != ZERO_F16 && dtype != ZERO_BF16) ||
         (n > 0 && (!g || !master || !m || !v || !half_out)))
         return ZERO_EINVAL;
-    if (!aligned16(g) || !aligned16(master) || !aligned16(m) || !aligned16(v) ||
+    if (!aligned32(g) || !aligned32(master) || !aligned32(m) || !aligned32(v) ||
         !aligned16(half_out) || (reinterpret_cast<uintptr_t>(state_dev) & 7u))
         return ZERO_EALIGN;
     if (n == 0)

@@ -63,7 +63,7 @@ const char *zero_strerror(int code)
     switch (code) {
     case ZERO_OK: return "ok";
     case ZERO_EINVAL: return "invalid argument";
-    case ZERO_EALIGN: return "buffer not 16-byte aligned";
+    case ZERO_EALIGN: return "buffer not aligned (32 bytes for fp32, 16 for half)";
     case ZERO_ESPACE: return "workspace too small";
     default: return code <= ZERO_ECUDA_BASE ? "CUDA launch failed" : "unknown error";
     }

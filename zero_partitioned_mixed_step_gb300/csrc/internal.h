@@ -13,6 +13,7 @@ constexpr int kMaxCtas = 4096;     // upper bound on CTAs of one reduction grid
 constexpr int kWsHeader = 256;     // bytes at the start of the workspace (unused header)
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 inline int cuda_error(int err) { return ZERO_ECUDA_BASE - err; }
 

@@ -21,32 +21,67 @@
 namespace zs {
 
 // ------------------------------------------------------------------ memory
+//
+// Every stream is touched once per step and a step moves far more than the
+// L2, so all accesses skip L1 and are marked evict-first in L2.  16-byte
+// accesses take the hint through an L2 cache policy; 256-bit accesses carry
+// it directly.
 
-// Gradient streams are read once: non-coherent path, no L1 allocation.
-__device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16 bytes of one rank's gradient (read-only during the kernel).
+__device__ __forceinline__ uint4 ld_stream(const uint16_t *p, uint64_t pol)
 {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
+        : "l"(p), "l"(pol));
     return r;
 }
 
-// Optimizer state may be updated in place by the same thread, so it is read
-// through the coherent path (evict-first).
-__device__ __forceinline__ float4 ld_state(const float *p)
+// 8 fp32 values (32 bytes, 32-byte aligned) in one 256-bit access.  The
+// coherent path is used because a clipped step may update the state in place.
+__device__ __forceinline__ void load8(const float *p, float x[8])
+{
+    uint32_t u[8];
+    asm("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7])
+        : "l"(p));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        x[i] = __uint_as_float(u[i]);
+}
+
+__device__ __forceinline__ void store8(float *p, const float x[8])
+{
+    asm volatile(
+        "st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+        :
+        : "l"(p), "r"(__float_as_uint(x[0])), "r"(__float_as_uint(x[1])),
+          "r"(__float_as_uint(x[2])), "r"(__float_as_uint(x[3])), "r"(__float_as_uint(x[4])),
+          "r"(__float_as_uint(x[5])), "r"(__float_as_uint(x[6])), "r"(__float_as_uint(x[7]))
+        : "memory");
+}
+
+// 16 bytes of half-precision parameters.
+__device__ __forceinline__ void st_half8(uint16_t *p, uint4 v, uint64_t pol)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// 4 fp32 values (16-byte aligned).
+__device__ __forceinline__ float4 ld_state4(const float *p)
 {
     return __ldcs(reinterpret_cast<const float4 *>(p));
-}
-
-__device__ __forceinline__ void st_state(float *p, float4 v)
-{
-    __stcs(reinterpret_cast<float4 *>(p), v);
-}
-
-__device__ __forceinline__ void st_half8(uint16_t *p, uint4 v)
-{
-    __stcs(reinterpret_cast<uint4 *>(p), v);
 }
 
 // ------------------------------------------------------------------ conversions
@@ -108,7 +143,7 @@ struct GradTable {
 // batches of up to 16 ranks before they are summed; W == 0: `world` at run time.
 template <int DT, int W, int MAXW>
 __device__ __forceinline__ void reduce_unit(const GradTable<MAXW> &t, int world, int64_t gi,
-                                            float acc[8])
+                                            float acc[8], uint64_t pol)
 {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -120,7 +155,7 @@ __device__ __forceinline__ void reduce_unit(const GradTable<MAXW> &t, int world,
             uint4 x[CH];
 #pragma unroll
             for (int j = 0; j < CH; ++j)
-                x[j] = ld_stream(t.p[q0 + j] + gi);
+                x[j] = ld_stream(t.p[q0 + j] + gi, pol);
 #pragma unroll
             for (int j = 0; j < CH; ++j)
                 add_half8<DT>(acc, x[j]);
@@ -131,13 +166,13 @@ __device__ __forceinline__ void reduce_unit(const GradTable<MAXW> &t, int world,
             uint4 x[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                x[j] = ld_stream(t.p[q + j] + gi);
+                x[j] = ld_stream(t.p[q + j] + gi, pol);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 add_half8<DT>(acc, x[j]);
         }
         for (; q < world; ++q)
-            add_half8<DT>(acc, ld_stream(t.p[q] + gi));
+            add_half8<DT>(acc, ld_stream(t.p[q] + gi, pol));
     }
 }
 
@@ -184,10 +219,11 @@ __device__ __forceinline__ int64_t flat_of(const View &v, int r, int64_t k)
 }
 
 // Flat index f, state index si and gradient index gi of unit u.
+template <bool ALL>
 __device__ __forceinline__ void locate(const View &v, int64_t u, int64_t &f, int64_t &si,
                                        int64_t &gi)
 {
-    if (v.all_ranks) {
+    if constexpr (ALL) {
         f = si = gi = u * kUnit;
     } else {
         f = flat_of(v, v.rank, u);
@@ -275,19 +311,6 @@ __device__ __forceinline__ uint16_t round_half1(float w)
         return __half_as_ushort(__float2half_rn(w));
     else
         return __bfloat16_as_ushort(__float2bfloat16_rn(w));
-}
-
-__device__ __forceinline__ void load8(const float *p, float x[8])
-{
-    const float4 a = ld_state(p), b = ld_state(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
-__device__ __forceinline__ void store8(float *p, const float x[8])
-{
-    st_state(p, make_float4(x[0], x[1], x[2], x[3]));
-    st_state(p + 4, make_float4(x[4], x[5], x[6], x[7]));
 }
 
 // ------------------------------------------------------------------ sum of squares

@@ -32,7 +32,7 @@ struct StepParams {
     double *partials;                           // PASS1: one per CTA
 };
 
-template <int DT, int W, int MAXW, int MODE>
+template <int DT, int W, int MAXW, int MODE, bool ALL>
 __global__ void __launch_bounds__(kThreads)
     step_kernel(const __grid_constant__ StepParams<MAXW> p)
 {
@@ -62,17 +62,18 @@ __global__ void __launch_bounds__(kThreads)
     float *v_dst = cur ? p.vo0 : p.vo1;
     uint16_t *out = cur ? p.par0 : p.par1;
 
+    const uint64_t pol = evict_first_policy();
     bool bad = false;
     SumSq ss;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < vw.units; u += stride) {
         int64_t f, si, gi;
-        locate(vw, u, f, si, gi);
+        locate<ALL>(vw, u, f, si, gi);
         float g[8];
         if constexpr (MODE == M_PASS2_STAGED) {
             load8(p.stage + si, g);
         } else {
-            reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g);
+            reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g, pol);
             if constexpr (MODE == M_RS) {
                 store8(p.stage + si, g);
                 continue;
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
         store8(w_dst + si, w);
         store8(m_dst + si, m);
         store8(v_dst + si, v);
-        st_half8(out + f, pack_half8<DT>(w));
+        st_half8(out + f, pack_half8<DT>(w), pol);
     }
     if constexpr (MODE == M_FUSED || MODE == M_PASS1)
         flag_nonfinite(bad, &p.state->found_inf);
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(kThreads)
 template <int DT, int W, int MAXW, int MODE>
 int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
 {
-    auto kern = step_kernel<DT, W, MAXW, MODE>;
+    auto kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true>
+                                 : step_kernel<DT, W, MAXW, MODE, false>;
     const int target = target_ctas(reinterpret_cast<const void *>(kern));
     const int64_t want = (p.view.units + kThreads - 1) / kThreads;
     const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
@@ -271,7 +273,7 @@ extern "C" int zero_reduce_scatter_sum(const void *const *grads, int grads_are_s
         return rc;
     if (!g_out)
         return ZERO_EINVAL;
-    if (!aligned16(g_out))
+    if (!aligned32(g_out))
         return ZERO_EALIGN;
     if (layout->padded_numel == 0)
         return ZERO_OK;
@@ -300,7 +302,7 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
     for (int s = 0; s < 2; ++s) {
         if (!empty && (!master[s] || !m[s] || !v[s] || !params[s]))
             return ZERO_EINVAL;
-        if (!aligned16(master[s]) || !aligned16(m[s]) || !aligned16(v[s]) || !aligned16(params[s]))
+        if (!aligned32(master[s]) || !aligned32(m[s]) || !aligned32(v[s]) || !aligned16(params[s]))
             return ZERO_EALIGN;
     }
     if (!clip && !empty &&
@@ -308,7 +310,7 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
         return ZERO_EINVAL;  // a one-pass step needs distinct slots to be able to skip
     if (g_stage && !clip)
         return ZERO_EINVAL;
-    if ((g_stage && !aligned16(g_stage)) || !aligned16(ws) ||
+    if ((g_stage && !aligned32(g_stage)) || !aligned16(ws) ||
         (reinterpret_cast<uintptr_t>(state_dev) & 7u))
         return ZERO_EALIGN;
     if (ws_bytes < zero_workspace_bytes(layout->world))
