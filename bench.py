@@ -47,12 +47,20 @@ def algorithmic_bytes_per_elem(world: int, clip: bool, staged: bool) -> int:
     return b
 
 
-def kernel_source_hash() -> str:
+STEP_KERNEL_SOURCES = ("step.cu", "kernels.cuh", "internal.h")
+
+
+def kernel_source_hash(read=None) -> str:
+    """Hash of the sources the fused step kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "zero_partitioned_mixed_step_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for name in STEP_KERNEL_SOURCES:
+        if read is None:
+            with open(os.path.join(csrc, name), "rb") as f:
+                data = f.read()
+        else:
+            data = read(name)
+        h.update(name.encode() + data)
     return h.hexdigest()[:16]
 
 
