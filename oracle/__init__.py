@@ -106,8 +106,8 @@ def _lib(openmp: bool = False):
         lib.orc_unscale.argtypes = [P, I64, ctypes.c_float]
         lib.orc_any_nonfinite.argtypes = [P, I64]
         lib.orc_any_nonfinite.restype = ctypes.c_int
-        lib.orc_sumsq.argtypes = [P, I64, ctypes.c_double]
-        lib.orc_sumsq.restype = ctypes.c_double
+        lib.orc_sumsq.argtypes = [P, I64, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]
         lib.orc_scale.argtypes = [P, I64, ctypes.c_float]
         lib.orc_adam.argtypes = [P, P, P, P, I64, ctypes.POINTER(_Scalars)]
         _LIBS[openmp] = lib
@@ -318,8 +318,17 @@ def any_nonfinite(g: np.ndarray, openmp: bool = False) -> bool:
     return bool(_lib(openmp).orc_any_nonfinite(_ptr(g), g.size))
 
 
-def sumsq(g: np.ndarray, acc: float = 0.0) -> float:
-    return _lib(False).orc_sumsq(_ptr(g), g.size, acc)
+def sumsq(g: np.ndarray, acc: Tuple[float, float] = (0.0, 0.0)) -> Tuple[float, float]:
+    """Step (a5): continue the compensated sum of squares ``acc`` = (sum,
+    compensation) over g; ``sumsq_value`` turns it into a number."""
+    s = ctypes.c_double(acc[0])
+    c = ctypes.c_double(acc[1])
+    _lib(False).orc_sumsq(_ptr(g), g.size, ctypes.byref(s), ctypes.byref(c))
+    return (s.value, c.value)
+
+
+def sumsq_value(acc: Tuple[float, float]) -> float:
+    return acc[0] + acc[1]
 
 
 def scale(g: np.ndarray, c: float, openmp: bool = False) -> None:
@@ -372,11 +381,11 @@ def step(grads: Sequence[np.ndarray], dtype: int, lay: Layout, cfg: AdamCfg, st:
     if cfg.max_grad_norm > 0:                                        # (a5)
         total = 0.0
         for r in ranks:
-            acc = 0.0
+            acc = (0.0, 0.0)
             for rr, _, _, g in parts:
                 if rr == r:
                     acc = sumsq(g, acc)
-            total = total + acc
+            total = total + sumsq_value(acc)
         st.sumsq = total
         st.coef = clip_coef(total, cfg.max_grad_norm)
         if st.coef < 1.0:
@@ -397,12 +406,12 @@ def scan_scalars(grad_chunks, dtype: int, lay: Layout, inv_scale: float, want_su
     too large to hold at once.  ``grad_chunks(r, flat_start, n)`` returns the
     world gradient arrays for flat elements [flat_start, flat_start + n);
     chunks are taken in each rank's element order, so the sum of squares is
-    the same sequential sum ``step`` forms.  ``ranks``: the simulated ranks
+    the same compensated sum ``step`` forms.  ``ranks``: the simulated ranks
     (all by default)."""
     flag = False
     total = 0.0
     for r in (range(lay.world) if ranks is None else ranks):
-        acc = 0.0
+        acc = (0.0, 0.0)
         for fs, ln in lay.segments[r]:
             for chunk_start in range(fs, fs + ln, chunk):
                 n = min(chunk, fs + ln - chunk_start)
@@ -412,7 +421,7 @@ def scan_scalars(grad_chunks, dtype: int, lay: Layout, inv_scale: float, want_su
                 flag = flag or any_nonfinite(g, openmp)
                 if want_sumsq:
                     acc = sumsq(g, acc)
-        total = total + acc
+        total = total + sumsq_value(acc)
     return flag, total
 
 

@@ -68,8 +68,7 @@ static float half_to_f32(uint16_t x, int dtype)
 /*
  * Round a binary32 value to a format with `p` significant bits, minimum
  * normal exponent `emin`, maximum finite value (2 - 2^(1-p)) * 2^emax,
- * to nearest with ties to even.  The result is returned as the exact value
- * (a double) plus the encoded bits.
+ * to nearest with ties to even, and return the encoded bits.
  *
  * Method: every representable value of the target format with exponent e is
  * k * 2^(e - p + 1) for an integer k.  For finite |x| > 0 take
@@ -181,15 +180,28 @@ int orc_any_nonfinite(const float *g, int64_t n)
     return found;
 }
 
-/* Step (a5): acc + sum_j double(g_j) * double(g_j), sequential in j.
- * A double product of two binary32 values is exact. */
-double orc_sumsq(const float *g, int64_t n, double acc)
+/* Step (a5): the sum of squares sum_j g_j^2 behind the global L2 gradient norm
+ * ("zero-optimizer", "一. 优化前": gradient-norm computation over fused
+ * buffers), continued from (*sum, *comp).  Each square is exact in binary64; the squares are added in sequence with
+ * Neumaier's compensated summation (Kahan-Babuska), which keeps the rounding
+ * error of every addition in *comp, so *sum + *comp is within a few ulps of
+ * the exact sum for any length (a plain sequential binary64 sum drifts by
+ * ~1e-9 relative over 1e9 such terms). */
+void orc_sumsq(const float *g, int64_t n, double *sum, double *comp)
 {
+    double s = *sum, c = *comp;
     for (int64_t j = 0; j < n; ++j) {
         double d = (double)g[j];
-        acc = acc + d * d;
+        double t = d * d;
+        double u = s + t;
+        if (fabs(s) >= fabs(t))
+            c = c + ((s - u) + t);
+        else
+            c = c + ((t - u) + s);
+        s = u;
     }
-    return acc;
+    *sum = s;
+    *comp = c;
 }
 
 /* Step (a5), clip: g = g * c in binary32. */

@@ -20,7 +20,8 @@ C_MUTATIONS = [
      "acc = acc + half_to_f32(grads[world - 1 - q][offset + j], dtype);"),
     ("unscale divides", "g[j] = g[j] * inv_scale;", "g[j] = g[j] / inv_scale;"),
     ("overflow misses Inf", "found |= !isfinite(g[j]);", "found |= isnan(g[j]);"),
-    ("sumsq drops square", "acc = acc + d * d;", "acc = acc + d;"),
+    ("sumsq drops square", "double t = d * d;", "double t = d;"),
+    ("sumsq drops compensation", "*comp = c;", "*comp = 0.0;"),
     ("momentum uses w", "s->omb1 * g;", "s->omb1 * wj;"),
     ("momentum drops decay", "float mj = s->b1 * m[j] + s->omb1 * g;", "float mj = m[j] + s->omb1 * g;"),
     ("variance not squared", "s->omb2 * (g * g);", "s->omb2 * g;"),

@@ -15,7 +15,11 @@ INF_BITS = {synth.F16: 0x7C00, synth.BF16: 0x7F80}
 # half-precision parameters within 1 ulp; flags and layout bit-exact.
 RTOL = 1e-6
 ATOL = 1e-12
-SUMSQ_RTOL = 1e-9
+# The global sum of squares: the oracle's compensated sum is within a few
+# ulps of the exact value; the GPU adds exact per-unit squares (error-free
+# transformations in binary32) into binary64 per thread (~10^4 terms) and
+# then in a fixed tree, which bounds its error near 1e-14 relative.
+SUMSQ_RTOL = 1e-11
 
 
 def oracle_cfg(wl) -> oracle.AdamCfg:
