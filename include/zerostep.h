@@ -219,6 +219,35 @@ int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev
                    size_t ws_bytes, zero_stream_t stream);
 
 /*
+ * zero_grad_norm for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is an interface variant, not a step of the method.
+ * Some callers have no way to provide the workspace zero_grad_norm needs:
+ * plain-C plugins that are handed device pointers by a host framework but
+ * have no allocator of their own, code inside a framework whose caching
+ * allocator already owns the device memory (a direct cudaMalloc can fail
+ * there although the framework has free memory), and loops that cannot
+ * afford the device-wide synchronisation cudaMalloc and cudaFree can cause.
+ * This entry point allocates nothing and calls no allocating routine.
+ *  Result, arguments and summation order: as zero_grad_norm (same kernels,
+ *  same grid, so the same bits), without ws / ws_bytes.
+ *  Scratch: the per-CTA partial sums live in a library-owned static device
+ *  array of ZERO_NOALLOC_PARTIALS doubles (32 KiB) that every GPU which
+ *  loads the library holds until the process exits.  A call that would need
+ *  more partial sums than that returns ZERO_ESPACE (the grid of the
+ *  reduction is capped at ZERO_NOALLOC_PARTIALS CTAs, so no length of g is
+ *  rejected on current GPUs).  Every call writes each slot it reads, so
+ *  nothing has to be cleared between calls; but all calls share the array,
+ *  so calls that can overlap on the GPU (different streams, or different
+ *  host threads, without ordering between them) race and must not be issued.
+ *  Set-up: the first call on each device looks up the array's device
+ *  address for the current device (cudaGetSymbolAddress) and caches it; make
+ *  that first call before any stream capture.
+ */
+#define ZERO_NOALLOC_PARTIALS 4096
+int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *sumsq_dev,
+                           zero_stream_t stream);
+
+/*
  * Steps (a3), (a5 clip), (a6), (a7) on n elements in place, for the reduced
  * gradient g that zero_reduce_scatter_sum produced (not yet unscaled).
  * Reads from state_dev: loss_scale, t and the beta powers (the update is step

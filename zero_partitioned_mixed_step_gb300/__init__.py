@@ -25,7 +25,7 @@ __all__ = [
     "F16", "BF16", "MAX_WORLD", "AdamCfg", "Layout", "StepState", "ZeroError", "ZeroStep",
     "adam_cfg", "new_state", "read_state", "state_field_ptr", "zero_partition_layout",
     "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
-    "zero_grad_norm", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
+    "zero_grad_norm", "zero_grad_norm_noalloc", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
 ]
 
 _TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
@@ -132,6 +132,15 @@ def zero_grad_norm(g: torch.Tensor, inv_scale: float, sumsq_ptr: int, ws: torch.
     check("zero_grad_norm",
           lib().zero_grad_norm(_dev_ptr(g), g.numel(), inv_scale, sumsq_ptr, _dev_ptr(ws),
                                ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def zero_grad_norm_noalloc(g: torch.Tensor, inv_scale: float, sumsq_ptr: int,
+                           stream=None) -> None:
+    """zero_grad_norm without a workspace: the partial sums live in a small
+    library-owned device array (see include/zerostep.h)."""
+    check("zero_grad_norm_noalloc",
+          lib().zero_grad_norm_noalloc(_dev_ptr(g), g.numel(), inv_scale, sumsq_ptr,
+                                       _stream(stream)))
 
 
 def zero_adam_step(g: torch.Tensor, master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,

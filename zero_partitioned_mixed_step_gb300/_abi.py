@@ -15,6 +15,7 @@ EALIGN = -2
 ESPACE = -3
 ECUDA_BASE = -1000
 MAX_WORLD = 1024
+NOALLOC_PARTIALS = 4096
 
 
 class Layout(ctypes.Structure):
@@ -60,6 +61,7 @@ SIGNATURES = {
     "zero_reduce_scatter_sum": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _P, _P], _I),
     "zero_check_overflow": ([_P, _I64, ctypes.c_float, _P, _P], _I),
     "zero_grad_norm": ([_P, _I64, ctypes.c_float, _P, _P, ctypes.c_size_t, _P], _I),
+    "zero_grad_norm_noalloc": ([_P, _I64, ctypes.c_float, _P, _P], _I),
     "zero_adam_step": ([_P, _P, _P, _P, _P, _I, _I64, ctypes.POINTER(AdamCfg), _P, _P], _I),
     "zero_step_finalize": ([ctypes.POINTER(AdamCfg), _P, _I, _P], _I),
     "zero_step_fused": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _P, _P, _P, _P, _P,

@@ -1,6 +1,7 @@
 // The unfused entry points (zero_check_overflow, zero_grad_norm,
 // zero_adam_step, zero_step_finalize) and the small single-CTA kernels that
 // end a step.
+#include <atomic>
 #include <cmath>
 
 #include "kernels.cuh"
@@ -289,3 +290,70 @@ int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation norm
+//
+// zero_grad_norm_noalloc: the same two kernels as zero_grad_norm, with the
+// per-CTA partial sums in a library-owned device array instead of a
+// caller-provided workspace.
+
+namespace zs {
+
+// One slot per CTA of the sum-of-squares grid.  Every GPU that loads the
+// library holds this array (ZERO_NOALLOC_PARTIALS doubles, 32 KiB) until the
+// process exits.  In host code the name is only a host-side stand-in for
+// the device array: kernels must be given the address cudaGetSymbolAddress
+// returns for the current device.
+static __device__ __align__(256) double noalloc_partials[ZERO_NOALLOC_PARTIALS];
+
+constexpr int kNoallocDevices = 64;
+static std::atomic<double *> noalloc_ptr[kNoallocDevices];
+
+// The device address of noalloc_partials on device `dev` (the current
+// device), looked up on the first call for that device and cached.
+static int noalloc_scratch(int dev, double **out)
+{
+    if (dev >= 0 && dev < kNoallocDevices) {
+        double *p = noalloc_ptr[dev].load(std::memory_order_acquire);
+        if (p) {
+            *out = p;
+            return ZERO_OK;
+        }
+    }
+    void *addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, noalloc_partials);
+    if (e != cudaSuccess || !addr)
+        return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    if (dev >= 0 && dev < kNoallocDevices)
+        noalloc_ptr[dev].store(static_cast<double *>(addr), std::memory_order_release);
+    *out = static_cast<double *>(addr);
+    return ZERO_OK;
+}
+
+}  // namespace zs
+
+extern "C" int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale,
+                                      double *sumsq_dev, zero_stream_t stream)
+{
+    using namespace zs;
+    if (n < 0 || !sumsq_dev || (n > 0 && !g) || !(inv_scale > 0.0f) || !std::isfinite(inv_scale))
+        return ZERO_EINVAL;
+    if (!aligned32(g) || (reinterpret_cast<uintptr_t>(sumsq_dev) & 7u))
+        return ZERO_EALIGN;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_error(e);
+    double *partials = nullptr;
+    int rc = noalloc_scratch(dev, &partials);
+    if (rc)
+        return rc;
+    const int gx = grid_for(reinterpret_cast<const void *>(sumsq_kernel), n / kUnit);
+    if (gx > ZERO_NOALLOC_PARTIALS)
+        return ZERO_ESPACE;  // more CTAs than the static scratch has slots
+    sumsq_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, partials);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_error(e);
+    return launch_norm_finalize(partials, gx, 1, 0.0, nullptr, sumsq_dev, stream);
+}
