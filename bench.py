@@ -202,17 +202,15 @@ def make_group(wl, device):
 
 # --------------------------------------------------------------------------- CPU legs
 
-def oracle_sample_rate(wl, target_s: float = 12.0, sample_elems: int = 1 << 22):
-    """Time the CPU oracle (OpenMP build, all host cores) on a bounded sample
-    of the workload: the first ``sample_elems`` owned elements of one rank,
-    with all N_d gradient buffers, stepped repeatedly for ~target_s seconds.
-    Returns (params/s, threads, description)."""
+def oracle_sample(wl, sample_elems: int):
+    """The CPU oracle's inputs for a bounded sample of the workload: one
+    rank's first ``sample_elems`` owned elements with all N_d gradient
+    buffers (seeded like the GPU inputs)."""
     import numpy as np
     import oracle
     import synth
 
-    n = sample_elems
-    lay = oracle.layout((n * wl.world,), wl.world)  # a flat sample with the same N_d
+    lay = oracle.layout((sample_elems * wl.world,), wl.world)  # a flat sample, same N_d
     grads = [synth.fill_half(wl.grad_key(1, q), 0, lay.padded, wl.grad_sigma * wl.loss_scale,
                              wl.dtype) for q in range(wl.world)]
     cfg = oracle.AdamCfg(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
@@ -220,14 +218,29 @@ def oracle_sample_rate(wl, target_s: float = 12.0, sample_elems: int = 1 << 22):
                          max_grad_norm=wl.max_grad_norm, dynamic_scale=wl.dynamic_scale)
     st = oracle.State(loss_scale=wl.loss_scale)
     w = synth.fill_f32(wl.master_key(), 0, lay.owned, wl.master_sigma)
-    m = np.zeros_like(w)
-    v = np.zeros_like(w)
-    half = np.zeros(lay.padded, np.uint16)
-    oracle.step(grads, wl.dtype, lay, cfg, st, w, m, v, half, rank=0, openmp=True)  # warm
+    bufs = (w, np.zeros_like(w), np.zeros_like(w), np.zeros(lay.padded, np.uint16))
+
+    def step():
+        oracle.step(grads, wl.dtype, lay, cfg, st, *bufs, rank=0, openmp=True)
+    return step
+
+
+def sample_elems_for(wl) -> int:
+    """About 2^28 gradient values per sample step, at most 2^24 elements."""
+    return max(1 << 18, min(1 << 24, (1 << 28) // wl.world))
+
+
+def oracle_sample_rate(wl, target_s: float = 12.0):
+    """cpu_baseline: the oracle (OpenMP build, all host cores) on the bounded
+    sample, stepped for about target_s seconds.  Returns (params/s, threads,
+    description)."""
+    n = sample_elems_for(wl) // 4
+    step = oracle_sample(wl, n)
+    step()  # warm
     steps = 0
     t0 = time.perf_counter()
     while True:
-        oracle.step(grads, wl.dtype, lay, cfg, st, w, m, v, half, rank=0, openmp=True)
+        step()
         steps += 1
         el = time.perf_counter() - t0
         if el >= target_s:
@@ -239,18 +252,32 @@ def oracle_sample_rate(wl, target_s: float = 12.0, sample_elems: int = 1 << 22):
 
 
 def run_reference(args, wl):
-    """--impl reference: the CPU oracle on the host cores, same metric."""
+    """--impl reference: the CPU oracle on the host cores, same metric: W
+    untimed and K timed steps, each on the bounded sample of the workload."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rate, threads, desc = oracle_sample_rate(wl, target_s=max(6.0, 1.5 * args.steps))
+    n = sample_elems_for(wl)
+    step = oracle_sample(wl, n)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    rate = n * args.steps / el
     value = rate / 1e9
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"{args.steps} timed oracle steps (after {args.warmup} untimed) of one rank's first "
+            f"{n} elements with all {wl.world} gradient buffers "
+            f"({wl.world * n * 2 / 1e6:.0f} MB of gradients per step)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": wl.numel / rate * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "psi": wl.numel, "world": wl.world},
+        "config": {"workload": wl.name, "psi": wl.numel, "world": wl.world,
+                   "sample_elems": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -259,6 +286,19 @@ def run_reference(args, wl):
 
 
 # --------------------------------------------------------------------------- GPU leg
+
+def max_over_ranks(x: float) -> float:
+    """The largest value of x over the ranks of the process group (x itself
+    without one).  The benchmark takes the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
 
 def run_ours(args, wl):
     import torch
@@ -320,12 +360,8 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
     if distributed:
         dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    if distributed:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     st = z.read_state()
 
     # end to end: the same step through the public API from pinned host buffers
