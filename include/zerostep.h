@@ -50,7 +50,7 @@
  * Conventions for every entry point:
  *  - The caller allocates and owns every buffer; the library allocates no
  *    memory and keeps no state between calls other than read-only device
- *    properties.  Pointers named *_dev or documented as device pointers must
+ *    properties (SM counts, resident CTAs per kernel), cached on first use.  Pointers named *_dev or documented as device pointers must
  *    be CUDA device pointers of the current device; all others are host
  *    pointers read during the call only.
  *  - Device work is enqueued on `stream` (NULL = the legacy default stream)

@@ -16,6 +16,18 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libzerostep.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    """The CUDA compiler: on PATH, else under CUDA_HOME or /usr/local/cuda."""
+    found = shutil.which("nvcc")
+    if found:
+        return found
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    path = os.path.join(home, "bin", "nvcc")
+    if not os.path.exists(path):
+        raise RuntimeError("nvcc not found (install the CUDA toolkit or set CUDA_HOME)")
+    return path
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-I", INCLUDE, *ARCH]
 
@@ -46,7 +58,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = ["nvcc", *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -61,8 +73,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 print(log)
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=BUILD)
     os.close(fd)
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(shutil.which("nvcc"))), "lib64")
-    r = subprocess.run(["nvcc", "-shared", "-cudart", "shared", *ARCH, *objs,
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
+    r = subprocess.run([nvcc(), "-shared", "-cudart", "shared", *ARCH, *objs,
                         "-Xlinker", "-rpath", "-Xlinker", cuda_lib, "-o", tmp],
                        capture_output=True, text=True)
     if r.returncode != 0:

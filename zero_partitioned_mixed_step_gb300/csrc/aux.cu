@@ -8,16 +8,71 @@
 
 namespace zs {
 
-int target_ctas(const void *kernel)
+// Resident CTAs per SM of each kernel, looked up once per kernel (the value
+// depends only on the kernel and the architecture), and the SM count of each
+// device: both are read-only after the first launch, so launches do not pay
+// for the queries again.
+namespace {
+
+constexpr int kOccSlots = 512;
+struct OccSlot {
+    std::atomic<const void *> kernel{nullptr};
+    std::atomic<int> occ{0};
+};
+OccSlot occ_slots[kOccSlots];
+constexpr int kSmDevices = 64;
+std::atomic<int> sm_count[kSmDevices];
+
+int resident_ctas(const void *kernel)
 {
-    int dev = 0, sms = 0, occ = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 1;
+    const size_t h = (reinterpret_cast<uintptr_t>(kernel) >> 4) % kOccSlots;
+    for (size_t i = 0; i < kOccSlots; ++i) {
+        OccSlot &s = occ_slots[(h + i) % kOccSlots];
+        const void *k = s.kernel.load(std::memory_order_acquire);
+        if (k == kernel) {
+            const int occ = s.occ.load(std::memory_order_acquire);
+            if (occ > 0)
+                return occ;
+            break;  // another thread is filling this slot: query directly
+        }
+        if (k == nullptr) {
+            int occ = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) !=
+                    cudaSuccess || occ < 1)
+                return 1;
+            const void *expected = nullptr;
+            if (s.kernel.compare_exchange_strong(expected, kernel, std::memory_order_acq_rel))
+                s.occ.store(occ, std::memory_order_release);
+            return occ;
+        }
+    }
+    int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
         occ < 1)
         occ = 1;
-    const int64_t t = (int64_t)sms * occ;
+    return occ;
+}
+
+int device_sms()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (dev >= 0 && dev < kSmDevices && (sms = sm_count[dev].load(std::memory_order_acquire)) > 0)
+        return sms;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1)
+        return 1;
+    if (dev >= 0 && dev < kSmDevices)
+        sm_count[dev].store(sms, std::memory_order_release);
+    return sms;
+}
+
+}  // namespace
+
+int target_ctas(const void *kernel)
+{
+    const int64_t t = (int64_t)device_sms() * resident_ctas(kernel);
     return (int)(t > kMaxCtas ? kMaxCtas : t);
 }
 
