@@ -104,6 +104,7 @@ def _lib(openmp: bool = False):
         lib.orc_from_half_array.argtypes = [P, I64, ctypes.c_int, P]
         lib.orc_reduce_sum.argtypes = [P, ctypes.c_int, ctypes.c_int, I64, I64, P]
         lib.orc_unscale.argtypes = [P, I64, ctypes.c_float]
+        lib.orc_accumulate.argtypes = [P, P, I64]
         lib.orc_any_nonfinite.argtypes = [P, I64]
         lib.orc_any_nonfinite.restype = ctypes.c_int
         lib.orc_sumsq.argtypes = [P, I64, ctypes.POINTER(ctypes.c_double),
@@ -310,6 +311,12 @@ def reduce_sum(grads: Sequence[np.ndarray], dtype: int, offset: int, n: int,
     return out
 
 
+def accumulate(acc: np.ndarray, r: np.ndarray, openmp: bool = False) -> None:
+    """acc += r element-wise in binary32 (one micro-step into the accumulator)."""
+    assert acc.dtype == np.float32 and r.dtype == np.float32 and acc.size == r.size
+    _lib(openmp).orc_accumulate(_ptr(acc), _ptr(r), acc.size)
+
+
 def unscale(g: np.ndarray, inv_scale: float, openmp: bool = False) -> None:
     _lib(openmp).orc_unscale(_ptr(g), g.size, inv_scale)
 
@@ -445,3 +452,73 @@ def window_step(grads: Sequence[np.ndarray], dtype: int, cfg: AdamCfg, st: State
     sc = step_scalars(cfg, st)
     adam(g, master, m, v, sc)
     return f32_to_half(master, dtype)
+
+
+# --------------------------------------------------------------------------
+# Gradient accumulation (next row f2)
+# --------------------------------------------------------------------------
+
+def reduce_scatter_accumulate(grads: Sequence[np.ndarray], dtype: int, lay: Layout,
+                              acc: np.ndarray, add: bool, rank: Optional[int] = None,
+                              grads_are_slices: bool = False, openmp: bool = False) -> None:
+    """One micro-step: acc = (acc if add else 0) + reduce-scatter sum.
+
+    "DeepSpeed ZeRO", "ZeRO-2 在梯度累积场景下的通信量": with gradient
+    accumulation ZeRO-2 reduce-scatters after every backward and accumulates
+    its 1/N_d slice.  The micro-step's sum over ranks is formed first (from
+    +0, ascending rank order), then added to the accumulator in binary32.
+    ``acc`` is flat (rank None) or rank r's elements in order (rank r)."""
+    for r in _ranks(lay, rank):
+        local = 0
+        for fs, ln in lay.segments[r]:
+            goff = local if (rank is not None and grads_are_slices) else fs
+            red = reduce_sum(grads, dtype, goff, ln, openmp)
+            si = fs if rank is None else local
+            if add:
+                accumulate(acc[si:si + ln], red, openmp)
+            else:
+                acc[si:si + ln] = red
+            local += ln
+
+
+def step_accumulated(acc: np.ndarray, dtype: int, lay: Layout, cfg: AdamCfg, st: State,
+                     master: np.ndarray, m: np.ndarray, v: np.ndarray, half: np.ndarray,
+                     rank: Optional[int] = None, openmp: bool = False) -> None:
+    """The step of ``step`` with the gradient taken from an fp32 accumulator
+    (the sum of the micro-steps' reduced, still scaled gradients) instead of
+    the N_d half-precision buffers: unscale, overflow test, clip, Adam, cast,
+    commit, in the same order."""
+    ranks = _ranks(lay, rank)
+    inv_s = f32(1.0 / st.loss_scale)
+    parts = []
+    for r in ranks:
+        local = 0
+        for fs, ln in lay.segments[r]:
+            si = fs if rank is None else local
+            g = np.array(acc[si:si + ln], dtype=np.float32, copy=True)
+            unscale(g, inv_s, openmp)
+            parts.append((r, fs, si, g))
+            local += ln
+    if any(any_nonfinite(g, openmp) for _, _, _, g in parts):
+        skip(cfg, st)
+        return
+    if cfg.max_grad_norm > 0:
+        total = 0.0
+        for r in ranks:
+            a = (0.0, 0.0)
+            for rr, _, _, g in parts:
+                if rr == r:
+                    a = sumsq(g, a)
+            total = total + sumsq_value(a)
+        st.sumsq = total
+        st.coef = clip_coef(total, cfg.max_grad_norm)
+        if st.coef < 1.0:
+            for _, _, _, g in parts:
+                scale(g, st.coef, openmp)
+    sc = step_scalars(cfg, st)
+    for _, fs, si, g in parts:
+        n = g.size
+        adam(g, master[si:si + n], m[si:si + n], v[si:si + n], sc, openmp)
+        half[fs:fs + n] = f32_to_half(master[si:si + n], dtype, openmp)
+    commit(cfg, st)
+

@@ -161,6 +161,18 @@ void orc_reduce_sum(const uint16_t *const *grads, int world, int dtype, int64_t 
     }
 }
 
+/* Gradient accumulation over micro-steps (next row f2): acc[j] = acc[j] + r[j]
+ * in binary32, where r is one micro-step's reduce-scattered sum.  "DeepSpeed
+ * ZeRO", "ZeRO-2 在梯度累积场景下的通信量": ZeRO-2 reduce-scatters after every
+ * backward and accumulates its 1/N_d slice; the memory section of the same
+ * page lists the optional fp32 gradient copy used to accumulate in fp32. */
+void orc_accumulate(float *acc, const float *r, int64_t n)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j)
+        acc[j] = acc[j] + r[j];
+}
+
 /* Step (a3): unscale by the loss scale S; inv_scale = 1/S (a power of two). */
 void orc_unscale(float *g, int64_t n, float inv_scale)
 {

@@ -502,8 +502,95 @@ def pin_layout():
     assert lay.padded == 321 * 25_000_000 + 5_261_312
 
 
+# ----------------------------------------------------------------- gradient accumulation
+
+def pin_accumulate_exact():
+    """K micro-steps of reduce-scatter into an fp32 accumulator: with values
+    on a coarse grid every sum is exact, so the accumulator must equal the
+    exact rational sum over micro-steps and ranks (all ranks' partitions and
+    one rank's view with slice buffers)."""
+    rnd = random.Random(17)
+    for world, psi, K in ((3, 200, 3), (4, 65, 5), (1, 8, 2)):
+        lay = oracle.layout([psi], world, align=8)
+        exact = [Fraction(0)] * lay.padded
+        acc = np.zeros(lay.padded, np.float32)
+        acc_r = np.zeros(lay.owned, np.float32)
+        idx = np.arange(lay.segments[world - 1][0][0], lay.segments[world - 1][0][0] + lay.owned)
+        for k in range(K):
+            vals = [[rnd.randint(-50, 50) * 2.0 ** rnd.randint(-10, -4) if j < psi else 0.0
+                     for j in range(lay.padded)] for _ in range(world)]
+            grads = [torch.tensor(v).to(torch.bfloat16).view(torch.int16).numpy()
+                     .view(np.uint16).copy() for v in vals]
+            for v in vals:
+                for j, x in enumerate(v):
+                    exact[j] += Fraction(float(torch.tensor(x).to(torch.bfloat16).float()))
+            oracle.reduce_scatter_accumulate(grads, oracle.BF16, lay, acc, k > 0)
+            oracle.reduce_scatter_accumulate([g[idx].copy() for g in grads], oracle.BF16, lay,
+                                             acc_r, k > 0, rank=world - 1, grads_are_slices=True)
+        assert all(Fraction(float(acc[j])) == exact[j] for j in range(lay.padded))
+        assert np.array_equal(acc_r, acc[idx])
+
+
+def pin_accumulate_order():
+    """A micro-step's ranks are summed first and the sum is added to the
+    accumulator once: 2^24 + (1 + 1) = 2^24 + 2 exactly, whereas adding the
+    ranks one at a time into the accumulator would lose both ones."""
+    lay = oracle.layout([8], 2, align=8)
+    acc = np.zeros(lay.padded, np.float32)
+    big = [torch.full((lay.padded,), 2.0 ** 24).to(torch.bfloat16), torch.zeros(lay.padded).to(torch.bfloat16)]
+    one = [torch.ones(lay.padded).to(torch.bfloat16)] * 2
+    for k, gs in enumerate((big, one)):
+        grads = [g.view(torch.int16).numpy().view(np.uint16).copy() for g in gs]
+        oracle.reduce_scatter_accumulate(grads, oracle.BF16, lay, acc, k > 0)
+    assert np.all(acc == np.float32(2.0 ** 24 + 2))
+
+
+def pin_accumulated_step():
+    """One micro-step accumulated and then stepped equals the plain step bit
+    for bit (flat, bucketed and one-rank views, with and without the clip); a
+    NaN in any micro-step skips the whole step."""
+    for world, numels, bucket, rank, clip in ((4, (3000, 100), 0, None, 0.0),
+                                               (3, (5000, 77), 1536, None, 0.5),
+                                               (4, (4096,), 0, 2, 0.0), (3, (5000, 77), 1536, 1, 0.0)):
+        lay, grads, master0 = _random_problem(world, numels, oracle.F16, world + 40, bucket=bucket)
+        cfg = oracle.AdamCfg(weight_decay=0.01, max_grad_norm=clip)
+        idx = (np.arange(lay.padded) if rank is None else
+               np.concatenate([np.arange(fs, fs + ln) for fs, ln in lay.segments[rank]]))
+        outs = []
+        for accumulated in (False, True):
+            w, m, v = master0[idx].copy(), np.zeros(idx.size, np.float32), np.zeros(idx.size, np.float32)
+            half = np.zeros(lay.padded, np.uint16)
+            st = oracle.State(loss_scale=1024.0)
+            for _ in range(2):
+                if accumulated:
+                    acc = np.zeros(idx.size, np.float32)
+                    oracle.reduce_scatter_accumulate(grads, oracle.F16, lay, acc, False, rank=rank)
+                    oracle.step_accumulated(acc, oracle.F16, lay, cfg, st, w, m, v, half, rank=rank)
+                else:
+                    oracle.step(grads, oracle.F16, lay, cfg, st, w, m, v, half, rank=rank)
+            outs.append((w, m, v, half, st.t, st.sumsq))
+        for a, b in zip(outs[0][:4], outs[1][:4]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+        assert outs[0][4:] == outs[1][4:]
+    lay, grads, master0 = _random_problem(2, (1000,), oracle.F16, 5)
+    cfg = oracle.AdamCfg()
+    w, m, v = master0.copy(), np.zeros_like(master0), np.zeros_like(master0)
+    half = np.zeros(lay.padded, np.uint16)
+    st = oracle.State(loss_scale=1024.0)
+    acc = np.zeros(lay.padded, np.float32)
+    bad = [g.copy() for g in grads]
+    bad[1][10] = 0x7E00
+    oracle.reduce_scatter_accumulate(bad, oracle.F16, lay, acc, False)
+    oracle.reduce_scatter_accumulate(grads, oracle.F16, lay, acc, True)
+    before = (w.copy(), m.copy(), v.copy())
+    oracle.step_accumulated(acc, oracle.F16, lay, cfg, st, w, m, v, half)
+    assert st.overflow == 1 and st.t == 0
+    assert all(np.array_equal(a, b) for a, b in zip(before, (w, m, v)))
+
+
 ALL_PINS = [pin_memory_closed_forms, pin_decode_exhaustive, pin_encode_structured,
             pin_reduce_bruteforce, pin_reduce_order, pin_unscale_exact, pin_overflow_detect,
             pin_sumsq, pin_clip_coef, pin_adam_first_step, pin_adam_constant_grad,
             pin_adam_literal_form, pin_vs_torch, pin_partition_concat, pin_skip_invariance,
-            pin_loss_scale_growth, pin_clip, pin_layout]
+            pin_loss_scale_growth, pin_clip, pin_layout, pin_accumulate_exact,
+            pin_accumulate_order, pin_accumulated_step]

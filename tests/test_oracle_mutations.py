@@ -36,6 +36,7 @@ C_MUTATIONS = [
     ("encode rounds half up", "double k = rint(q);", "double k = floor(q + 0.5);"),
     ("encode no overflow to Inf", "if (e > emax)", "if (e > emax + 1)"),
     ("bf16 decode shift", "(uint32_t)b << 16;", "(uint32_t)b << 15;"),
+    ("accumulate overwrites", "acc[j] = acc[j] + r[j];", "acc[j] = r[j];"),
 ]
 
 
@@ -76,7 +77,8 @@ def test_c_mutation_is_caught(name, text, repl, tmp_path, monkeypatch):
             real = saved.get(omp) or oracle._lib(omp)
             for fn in ("orc_f16_to_f32", "orc_bf16_to_f32", "orc_f32_to_f16", "orc_f32_to_bf16",
                        "orc_to_half_array", "orc_from_half_array", "orc_reduce_sum", "orc_unscale",
-                       "orc_any_nonfinite", "orc_sumsq", "orc_scale", "orc_adam"):
+                       "orc_any_nonfinite", "orc_sumsq", "orc_scale", "orc_adam",
+                       "orc_accumulate"):
                 f = getattr(lib, fn)
                 f.argtypes = getattr(real, fn).argtypes
                 f.restype = getattr(real, fn).restype
