@@ -103,6 +103,7 @@ def _lib(openmp: bool = False):
         lib.orc_to_half_array.argtypes = [P, I64, ctypes.c_int, P]
         lib.orc_from_half_array.argtypes = [P, I64, ctypes.c_int, P]
         lib.orc_reduce_sum.argtypes = [P, ctypes.c_int, ctypes.c_int, I64, I64, P]
+        lib.orc_reduce_sum_half.argtypes = [P, ctypes.c_int, ctypes.c_int, I64, I64, P]
         lib.orc_unscale.argtypes = [P, I64, ctypes.c_float]
         lib.orc_accumulate.argtypes = [P, P, I64]
         lib.orc_any_nonfinite.argtypes = [P, I64]
@@ -301,13 +302,16 @@ def commit(cfg: AdamCfg, st: State) -> None:
 # --------------------------------------------------------------------------
 
 def reduce_sum(grads: Sequence[np.ndarray], dtype: int, offset: int, n: int,
-               openmp: bool = False) -> np.ndarray:
-    """Step (a2): g[j] = sum_q float(grads[q][offset + j]) in ascending q."""
+               openmp: bool = False, half_reduce: bool = False) -> np.ndarray:
+    """Step (a2): g[j] = sum_q float(grads[q][offset + j]) in ascending q, in
+    binary32, or with ``half_reduce`` in the gradient's half type (every
+    partial sum rounded to nearest even)."""
     arr = (ctypes.c_void_p * len(grads))(*[_ptr(g) for g in grads])
     for g in grads:
         assert g.dtype == np.uint16 and g.size >= offset + n
     out = np.empty(n, np.float32)
-    _lib(openmp).orc_reduce_sum(arr, len(grads), dtype, offset, n, _ptr(out))
+    fn = _lib(openmp).orc_reduce_sum_half if half_reduce else _lib(openmp).orc_reduce_sum
+    fn(arr, len(grads), dtype, offset, n, _ptr(out))
     return out
 
 
@@ -361,7 +365,7 @@ def _ranks(lay: Layout, rank: Optional[int]) -> List[int]:
 def step(grads: Sequence[np.ndarray], dtype: int, lay: Layout, cfg: AdamCfg, st: State,
          master: np.ndarray, m: np.ndarray, v: np.ndarray, half: np.ndarray,
          rank: Optional[int] = None, grads_are_slices: bool = False,
-         openmp: bool = False) -> None:
+         openmp: bool = False, half_reduce: bool = False) -> None:
     """One partitioned mixed-precision step, in place.
 
     ``rank`` None simulates all ranks: ``grads[q]`` are the ranks' full padded
@@ -369,7 +373,8 @@ def step(grads: Sequence[np.ndarray], dtype: int, lay: Layout, cfg: AdamCfg, st:
     flat positions).  ``rank`` = r simulates rank r alone: master/m/v hold the
     elements r owns, in order, and ``grads[q]`` are either full buffers or
     (``grads_are_slices``) only the elements r owns.  ``half`` is always the
-    full flat parameter buffer in the all-gather layout.
+    full flat parameter buffer in the all-gather layout.  ``half_reduce``
+    reduces in the gradient's half type (see ``reduce_sum``).
     """
     ranks = _ranks(lay, rank)
     inv_s = f32(1.0 / st.loss_scale)
@@ -378,7 +383,7 @@ def step(grads: Sequence[np.ndarray], dtype: int, lay: Layout, cfg: AdamCfg, st:
         local = 0
         for fs, ln in lay.segments[r]:
             goff = local if (rank is not None and grads_are_slices) else fs
-            g = reduce_sum(grads, dtype, goff, ln, openmp)          # (a2)
+            g = reduce_sum(grads, dtype, goff, ln, openmp, half_reduce)  # (a2)
             unscale(g, inv_s, openmp)                                # (a3)
             parts.append((r, fs, fs if rank is None else local, g))
             local += ln
@@ -408,7 +413,7 @@ def step(grads: Sequence[np.ndarray], dtype: int, lay: Layout, cfg: AdamCfg, st:
 
 def scan_scalars(grad_chunks, dtype: int, lay: Layout, inv_scale: float, want_sumsq: bool,
                  openmp: bool = False, ranks: Optional[Sequence[int]] = None,
-                 chunk: int = 1 << 24) -> Tuple[bool, float]:
+                 chunk: int = 1 << 24, half_reduce: bool = False) -> Tuple[bool, float]:
     """The step's global scalars (overflow flag, sum of squares) for gradients
     too large to hold at once.  ``grad_chunks(r, flat_start, n)`` returns the
     world gradient arrays for flat elements [flat_start, flat_start + n);
@@ -423,7 +428,7 @@ def scan_scalars(grad_chunks, dtype: int, lay: Layout, inv_scale: float, want_su
             for chunk_start in range(fs, fs + ln, chunk):
                 n = min(chunk, fs + ln - chunk_start)
                 gs = grad_chunks(r, chunk_start, n)
-                g = reduce_sum(gs, dtype, 0, n, openmp)
+                g = reduce_sum(gs, dtype, 0, n, openmp, half_reduce)
                 unscale(g, inv_scale, openmp)
                 flag = flag or any_nonfinite(g, openmp)
                 if want_sumsq:
@@ -433,15 +438,15 @@ def scan_scalars(grad_chunks, dtype: int, lay: Layout, inv_scale: float, want_su
 
 
 def window_step(grads: Sequence[np.ndarray], dtype: int, cfg: AdamCfg, st: State, flag: bool,
-                total_sumsq: float, master: np.ndarray, m: np.ndarray, v: np.ndarray
-                ) -> Optional[np.ndarray]:
+                total_sumsq: float, master: np.ndarray, m: np.ndarray, v: np.ndarray,
+                half_reduce: bool = False) -> Optional[np.ndarray]:
     """Steps (a2)-(a7) for one contiguous window of a rank's elements, given
     the step's global scalars (the update is element-wise once they are known:
     "DeepSpeed ZeRO", ZeRO Stage 2, the per-element independence of Adam).
     ``grads[q]`` hold the window's gradient elements.  Updates master/m/v in
     place and returns the half output, or None when the step is skipped.
     Does not advance ``st``; call ``skip``/``commit`` once per step."""
-    g = reduce_sum(grads, dtype, 0, master.size)
+    g = reduce_sum(grads, dtype, 0, master.size, half_reduce=half_reduce)
     unscale(g, f32(1.0 / st.loss_scale))
     if flag:
         return None
@@ -460,7 +465,8 @@ def window_step(grads: Sequence[np.ndarray], dtype: int, cfg: AdamCfg, st: State
 
 def reduce_scatter_accumulate(grads: Sequence[np.ndarray], dtype: int, lay: Layout,
                               acc: np.ndarray, add: bool, rank: Optional[int] = None,
-                              grads_are_slices: bool = False, openmp: bool = False) -> None:
+                              grads_are_slices: bool = False, openmp: bool = False,
+                              half_reduce: bool = False) -> None:
     """One micro-step: acc = (acc if add else 0) + reduce-scatter sum.
 
     "DeepSpeed ZeRO", "ZeRO-2 在梯度累积场景下的通信量": with gradient
@@ -472,7 +478,7 @@ def reduce_scatter_accumulate(grads: Sequence[np.ndarray], dtype: int, lay: Layo
         local = 0
         for fs, ln in lay.segments[r]:
             goff = local if (rank is not None and grads_are_slices) else fs
-            red = reduce_sum(grads, dtype, goff, ln, openmp)
+            red = reduce_sum(grads, dtype, goff, ln, openmp, half_reduce)
             si = fs if rank is None else local
             if add:
                 accumulate(acc[si:si + ln], red, openmp)

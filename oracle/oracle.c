@@ -72,23 +72,23 @@ static float half_to_f32(uint16_t x, int dtype)
  *
  * Method: every representable value of the target format with exponent e is
  * k * 2^(e - p + 1) for an integer k.  For finite |x| > 0 take
- * e = max(floor(log2 |x|), emin) and q = |x| / 2^(e - p + 1); q has at most
- * 24 significant bits, so it is exact in double, and rint() (the default
- * rounding mode is round-half-even) gives the nearest k with ties to even.
+ * e = max(floor(log2 |x|), emin) and q = |x| / 2^(e - p + 1); scaling by a
+ * power of two is exact in double, and rint() (the default rounding mode is
+ * round-half-even) gives the nearest k with ties to even.  x is a double, so
+ * both binary32 values and exact sums of two half-precision values are
+ * rounded once.
  * k = 2^p means the value rounded up into the next binade.
  */
-static uint16_t round_to_format(float x, int p, int emin, int emax, int bias, uint16_t qnan)
+static uint16_t round_to_format(double x, int p, int emin, int emax, int bias, uint16_t qnan)
 {
-    uint32_t ux;
-    memcpy(&ux, &x, sizeof ux);
-    uint16_t sign = (uint16_t)((ux >> 31) << 15);
+    uint16_t sign = (uint16_t)(signbit(x) ? 0x8000u : 0u);
     int fbits = p - 1; /* stored fraction bits */
     if (isnan(x))
         return (uint16_t)(sign | qnan);
     uint16_t inf_bits = (uint16_t)(((1u << (15 - fbits)) - 1u) << fbits);
     if (isinf(x))
         return (uint16_t)(sign | inf_bits);
-    double ax = fabs((double)x);
+    double ax = fabs(x);
     if (ax == 0.0)
         return sign;
     int e2;
@@ -171,6 +171,35 @@ void orc_accumulate(float *acc, const float *r, int64_t n)
 #pragma omp parallel for schedule(static)
     for (int64_t j = 0; j < n; ++j)
         acc[j] = acc[j] + r[j];
+}
+
+/*
+ * Step (a2) with the reduction itself in half precision (next row f3): the
+ * running sum is kept in the gradient's type and rounded to nearest even
+ * after every addition, in ascending rank order from +0, as a half-precision
+ * reduce-scatter produces it ("DeepSpeed ZeRO", ZeRO Stage 2: the fp32
+ * gradient slice is made from the reduce-scattered BF16 gradient).  Each
+ * addition forms the sum of two half values in binary64 and rounds it to the
+ * half type: the binary64 sum is exact for fp16 (exponents span < 42 bits);
+ * for bf16 it is exact unless the two exponents differ by more than 45, and
+ * then the smaller value lies far below half an ulp of the result, so the
+ * single rounding still gives the correctly rounded half-precision sum.
+ * Overflow gives +-Inf and Inf + -Inf gives NaN.
+ */
+void orc_reduce_sum_half(const uint16_t *const *grads, int world, int dtype, int64_t offset,
+                         int64_t n, float *g)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int q = 0; q < world; ++q) {
+            double exact = acc + (double)half_to_f32(grads[q][offset + j], dtype);
+            uint16_t h = dtype == ORC_F16 ? round_to_format(exact, 11, -14, 15, 15, 0x7E00)
+                                          : round_to_format(exact, 8, -126, 127, 127, 0x7FC0);
+            acc = (double)half_to_f32(h, dtype);
+        }
+        g[j] = (float)acc;
+    }
 }
 
 /* Step (a3): unscale by the loss scale S; inv_scale = 1/S (a power of two). */

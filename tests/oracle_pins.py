@@ -588,9 +588,50 @@ def pin_accumulated_step():
     assert all(np.array_equal(a, b) for a, b in zip(before, (w, m, v)))
 
 
+# ----------------------------------------------------------------- half-precision reduction
+
+def pin_half_reduce():
+    """The reduction in the gradient's own half type rounds every partial sum
+    to nearest even, in ascending rank order: fp16 against numpy's correctly
+    rounded binary64 -> binary16 conversion of each exact partial sum
+    (subnormals and overflow included); bf16 on values whose binary32 sums
+    are exact, against torch's bf16 rounding; 2048 + 1 + 1 = 2048 in fp16
+    (2050 in the reverse order); 60000 + 60000 overflows to Inf in fp16
+    although it is finite in binary32."""
+    rng = np.random.default_rng(23)
+    for world in (1, 2, 3, 5, 8):
+        n = 4000
+        exps = rng.integers(-24, 16, size=(world, n))
+        vals = (rng.integers(-1023, 1024, size=(world, n)) * np.exp2(exps - 10.0)).astype(np.float16)
+        grads = [v.view(np.uint16).copy() for v in vals]
+        got = oracle.reduce_sum(grads, oracle.F16, 0, n, half_reduce=True)
+        acc = np.zeros(n, np.float16)
+        for q in range(world):
+            acc = (acc.astype(np.float64) + vals[q].astype(np.float64)).astype(np.float16)
+        want = acc.astype(np.float32)
+        same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+        assert same.all(), world
+        # bf16: exponents within a band of 12, so binary32 holds every exact sum
+        e = rng.integers(-20, -8, size=(world, n))
+        bv = torch.from_numpy((rng.integers(-127, 128, size=(world, n)) * np.exp2(e - 7.0))
+                              .astype(np.float32)).to(torch.bfloat16)
+        grads = [bv[q].view(torch.int16).numpy().view(np.uint16).copy() for q in range(world)]
+        got = oracle.reduce_sum(grads, oracle.BF16, 0, n, half_reduce=True)
+        acc = torch.zeros(n, dtype=torch.bfloat16)
+        for q in range(world):
+            acc = (acc.float() + bv[q].float()).to(torch.bfloat16)
+        assert np.array_equal(got.view(np.uint32), acc.float().numpy().view(np.uint32)), world
+    order = [np.array([x], np.float16).view(np.uint16) for x in (2048.0, 1.0, 1.0)]
+    assert oracle.reduce_sum(order, oracle.F16, 0, 1, half_reduce=True)[0] == 2048.0
+    assert oracle.reduce_sum(order[::-1], oracle.F16, 0, 1, half_reduce=True)[0] == 2050.0
+    big = [np.array([60000.0], np.float16).view(np.uint16)] * 2
+    assert np.isinf(oracle.reduce_sum(big, oracle.F16, 0, 1, half_reduce=True)[0])
+    assert oracle.reduce_sum(big, oracle.F16, 0, 1)[0] == 120000.0
+
+
 ALL_PINS = [pin_memory_closed_forms, pin_decode_exhaustive, pin_encode_structured,
             pin_reduce_bruteforce, pin_reduce_order, pin_unscale_exact, pin_overflow_detect,
             pin_sumsq, pin_clip_coef, pin_adam_first_step, pin_adam_constant_grad,
             pin_adam_literal_form, pin_vs_torch, pin_partition_concat, pin_skip_invariance,
             pin_loss_scale_growth, pin_clip, pin_layout, pin_accumulate_exact,
-            pin_accumulate_order, pin_accumulated_step]
+            pin_accumulate_order, pin_accumulated_step, pin_half_reduce]

@@ -37,6 +37,8 @@ C_MUTATIONS = [
     ("encode no overflow to Inf", "if (e > emax)", "if (e > emax + 1)"),
     ("bf16 decode shift", "(uint32_t)b << 16;", "(uint32_t)b << 15;"),
     ("accumulate overwrites", "acc[j] = acc[j] + r[j];", "acc[j] = r[j];"),
+    ("half reduce rounds only at the end", "acc = (double)half_to_f32(h, dtype);",
+     "acc = exact; (void)h;"),
 ]
 
 
@@ -78,7 +80,7 @@ def test_c_mutation_is_caught(name, text, repl, tmp_path, monkeypatch):
             for fn in ("orc_f16_to_f32", "orc_bf16_to_f32", "orc_f32_to_f16", "orc_f32_to_bf16",
                        "orc_to_half_array", "orc_from_half_array", "orc_reduce_sum", "orc_unscale",
                        "orc_any_nonfinite", "orc_sumsq", "orc_scale", "orc_adam",
-                       "orc_accumulate"):
+                       "orc_accumulate", "orc_reduce_sum_half"):
                 f = getattr(lib, fn)
                 f.argtypes = getattr(real, fn).argtypes
                 f.restype = getattr(real, fn).restype
