@@ -37,11 +37,16 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129e6  # GB300 L2
 
 
-def algorithmic_bytes_per_elem(world: int, clip: bool, staged: bool) -> int:
+def algorithmic_bytes_per_elem(world: int, clip: bool, staged: bool, micro: int = 1) -> int:
     """Bytes an ideal step moves per padded element: read the N_d half
     gradients, read and write fp32 master/m/v, write the half parameter.
     A clipped step needs a second pass: +8 (stage written and read) or
-    +2 N_d (gradients read again)."""
+    +2 N_d (gradients read again).  With gradient accumulation over micro > 1
+    micro-steps each micro-step reads the N_d gradients and writes the fp32
+    accumulator (all but the first also read it), and the step reads the
+    accumulator (twice with clipping) instead of the gradients."""
+    if micro > 1:
+        return micro * (2 * world + 8) - 4 + 4 + 26 + (4 if clip else 0)
     b = 2 * world + 24 + 2
     if clip:
         b += 8 if staged else 2 * world
@@ -338,7 +343,7 @@ def run_ours(args, wl):
             grads[q][i:i + 1].copy_(saved.pop((q, i)))
 
     clip = wl.max_grad_norm > 0
-    bpe = algorithmic_bytes_per_elem(wl.world, clip, z.g_stage is not None)
+    bpe = algorithmic_bytes_per_elem(wl.world, clip, z.g_stage is not None, wl.micro_steps)
     n_elems = L.padded_numel if wl.rank is None else L.owned_numel
     # A step that moves less than a few L2 sizes could be served from L2 on
     # the next step: then a 256 MB write flushes L2 between timed steps, and
@@ -347,8 +352,18 @@ def run_ours(args, wl):
     if n_elems * bpe < 4 * L2_BYTES:
         flush = torch.empty(64 << 20, dtype=torch.float32, device=device)
 
+    micro = wl.micro_steps
+
+    def one_step():
+        if micro > 1:  # gradient accumulation: the same buffers stand for every micro-step
+            for k in range(micro):
+                z.accumulate(grads, k > 0, stream)
+            z.step_accumulated(stream)
+        else:
+            z.step(grads, stream)
+
     for s in range(1, args.warmup + 1):
-        z.step(grads, stream)
+        one_step()
     torch.cuda.synchronize()
 
     nsteps = args.steps
@@ -366,7 +381,7 @@ def run_ours(args, wl):
             if flush is not None:
                 flush.fill_(float(s))
             ev[s - 1][0].record(stream)
-            z.step(grads, stream)
+            one_step()
             ev[s - 1][1].record(stream)
             after(s)
         t_end.record(stream)
@@ -393,7 +408,7 @@ def run_ours(args, wl):
     peak = peaks["hbm_gbs"]
     traffic = recorded_traffic(wl.name)
     rate, threads, desc = oracle_sample_rate(wl)
-    launches_per_step = 4 if clip else 2
+    launches_per_step = (4 if clip else 2) + (wl.micro_steps if wl.micro_steps > 1 else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world_size,
         "steps": nsteps, "warmup": args.warmup, "ms_per_step": total_ms / nsteps,
@@ -403,14 +418,18 @@ def run_ours(args, wl):
                    "world": wl.world, "grad_dtype": "f16" if wl.dtype == zs.F16 else "bf16",
                    "rank_view": wl.rank, "bucket": wl.bucket, "clip": clip,
                    "bytes_per_elem": bpe, "replicas": world_size,
+                   "micro_steps": wl.micro_steps,
                    "l2": ("no flush: each step streams %.1f GB (> 129 MB L2)" % (n_elems * bpe / 1e9)
                           if flush is None else
                           "L2 flushed (256 MB write) between timed steps; time = sum of steps"),
                    "skipped_steps": st.skipped},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_kind": f"{kind} hbm_gbs", "kernel": "step_kernel (fused, one pass)"
-                     if not clip else "step_kernel (two passes)",
+                     "peak_kind": f"{kind} hbm_gbs",
+                     "kernel": ("step_kernel (%s)" % ("fused, one pass" if not clip else
+                                                      "two passes"))
+                     + (" after %d accumulate passes" % wl.micro_steps
+                        if wl.micro_steps > 1 else ""),
                      "kernel_ms": kernel_ms, "bytes_per_launch": n_elems * bpe},
         "cpu_baseline": {"value": rate / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
@@ -435,13 +454,13 @@ def run_e2e(z, grads, wl, args, steps: int = 5):
     for h, g in zip(host, grads):
         h.copy_(g)
     stream = torch.cuda.current_stream()
-    z.step_from_host(host, grads, stream)  # warm-up
+    z.step_from_host(host, grads, stream, wl.micro_steps)  # warm-up
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        z.step_from_host(host, grads, stream)
+        z.step_from_host(host, grads, stream, wl.micro_steps)
     el = time.perf_counter() - t0
-    h2d = sum(g.numel() * g.element_size() for g in grads)
+    h2d = sum(g.numel() * g.element_size() for g in grads) * wl.micro_steps
     params = wl.numel if wl.rank is None else min(z.layout.owned_numel, wl.numel)
     del host
     return {"value": params * steps / el / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,

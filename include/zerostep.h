@@ -88,7 +88,19 @@ enum {
 
 #define ZERO_MAX_WORLD 1024
 
-typedef enum { ZERO_F16 = 0, ZERO_BF16 = 1 } zero_dtype;
+/* Gradient / parameter precision.  With ZERO_F16 or ZERO_BF16 the gradients
+ * are reduced in fp32.  The _HALF_REDUCE codes keep the same storage type but
+ * reduce in it: every partial sum over ranks is rounded to nearest even in
+ * the half type, in ascending rank order, as a half-precision reduce-scatter
+ * produces it ("DeepSpeed ZeRO", ZeRO Stage 2: the fp32 gradient slice is
+ * made from the reduce-scattered BF16 gradient); a partial sum beyond the
+ * type's range becomes +-Inf and skips the step. */
+typedef enum {
+    ZERO_F16 = 0,
+    ZERO_BF16 = 1,
+    ZERO_F16_HALF_REDUCE = 2,
+    ZERO_BF16_HALF_REDUCE = 3
+} zero_dtype;
 
 /*
  * Partition layout of the flat parameter vector (step a1).
@@ -217,6 +229,40 @@ int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *fla
  */
 int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
                    size_t ws_bytes, zero_stream_t stream);
+
+/*
+ * Gradient accumulation, one micro-step: the reduce-scatter sum of the N_d
+ * half-precision gradients (as zero_reduce_scatter_sum: fp32, ascending rank
+ * order from +0, not unscaled) added to an fp32 accumulator:
+ *   acc[j] = (add ? acc[j] : 0) + sum_q float(grads[q][.])
+ * (the micro-step's sum over ranks is formed first, then added once).
+ *  grads, grads_are_slices, dtype, layout, rank: as zero_reduce_scatter_sum.
+ *  acc: device fp32, padded_numel (rank = -1, flat order) or owned_numel
+ *  (rank = r, r's order), 32-byte aligned.  add = 0 starts a new accumulation.
+ * Pages: "DeepSpeed ZeRO", "ZeRO-2 在梯度累积场景下的通信量" (ZeRO-2 reduce-scatters
+ * after every backward and accumulates its 1/N_d slice) and the page's memory
+ * section (the optional fp32 gradient copy for accumulating in fp32).
+ */
+int zero_reduce_scatter_accumulate(const void *const *grads, int grads_are_slices,
+                                   zero_dtype dtype, const zero_layout *layout, int rank,
+                                   float *acc, int add, zero_stream_t stream);
+
+/*
+ * The whole step (a3)-(a8) with the gradient taken from an fp32 accumulator
+ * (after micro-steps of zero_reduce_scatter_accumulate) instead of the N_d
+ * half-precision buffers: unscale, overflow test (NaN/Inf in any micro-step
+ * skips the step), optional clip, Adam/AdamW, cast, commit.  dtype is the
+ * parameter buffer's type; acc, layout and rank as in
+ * zero_reduce_scatter_accumulate; master, m, v, params, cfg, state_dev, ws as
+ * zero_step_fused (one pass with distinct ping-pong slots without clipping;
+ * two passes over acc, slots may alias, with clipping).
+ * Pages: as zero_step_fused and zero_reduce_scatter_accumulate.
+ */
+int zero_step_fused_accumulated(const float *acc, zero_dtype dtype, const zero_layout *layout,
+                                int rank, float *const master[2], float *const m[2],
+                                float *const v[2], void *const params[2],
+                                const zero_adam_cfg *cfg, zero_step_state *state_dev, void *ws,
+                                size_t ws_bytes, zero_stream_t stream);
 
 /*
  * zero_grad_norm for callers that cannot allocate device memory.  The pages

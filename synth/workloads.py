@@ -73,6 +73,8 @@ class Workload:
     align: int = 64
     inject_every: int = 0                # inject +Inf at steps that are multiples of this
     inject_at: Tuple[Tuple[int, int, int], ...] = ()   # (step, rank, flat index)
+    micro_steps: int = 1                 # gradient-accumulation micro-steps per step
+    half_reduce: bool = False            # reduce in the gradients' half type, not fp32
 
     @property
     def numel(self) -> int:
@@ -84,8 +86,9 @@ class Workload:
     def master_key(self) -> int:
         return key(self.seed, 10_000)
 
-    def grad_key(self, step: int, q: int) -> int:
-        return key(self.grad_seed(step), q)
+    def grad_key(self, step: int, q: int, micro: int = 0) -> int:
+        """Rank q's gradient at a step (1-based) and micro-step (0-based)."""
+        return key(self.grad_seed(step), q + 1024 * micro)
 
     def injections(self, step: int) -> Tuple[Tuple[int, int], ...]:
         """(rank, flat index) pairs that receive +Inf before ``step`` (1-based)."""
@@ -135,4 +138,13 @@ ALL = (CFG1, CFG2, CFG3, CFG4, CFG5)
 # while the buffers hold ~4 GB of device memory.
 PROFILE_CFG3 = CFG3.replace(name="flat-64M-nd16-fp16-dynamic", numels=(64_000_000,))
 
-BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3,)}
+# Gradient accumulation (four micro-steps of reduce-scatter into an fp32
+# accumulator per optimizer step) on the 1.5B, 16-rank workload.
+ACCUM_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-accum4", micro_steps=4, steps=20,
+                          inject_every=0)
+
+# The 1.5B, 16-rank workload with the reduction in fp16 (each partial sum
+# rounded to fp16), as a half-precision reduce-scatter would produce it.
+HALFRED_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-halfreduce", half_reduce=True)
+
+BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, ACCUM_CFG3, HALFRED_CFG3)}

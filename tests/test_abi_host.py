@@ -35,7 +35,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(zs):
     names = declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 14, names
     so = ctypes.CDLL(zs._build.LIB)
     for n in names:
         assert hasattr(so, n), n

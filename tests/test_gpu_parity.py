@@ -279,3 +279,112 @@ def test_generators_agree():
         synth.gpu_round_half(x, out, dtype)
         assert np.array_equal(out.cpu().numpy().view(np.uint16),
                               synth.round_half(x.cpu().numpy(), dtype))
+
+
+# ----------------------------------------------------------------- gradient accumulation
+
+ACCUM = {
+    "flat-nd16-4micro": CFG3.replace(numels=(1_000_003,), steps=3, micro_steps=4,
+                                     inject_every=0, inject_at=((2, 3, 4321),)),
+    "gpt2-nd8-clip-3micro": SMALL["cfg2-small"].replace(steps=2, micro_steps=3),
+    "bucketed-rank-slices-2micro": EDGE["bucketed-rank-slices"].replace(micro_steps=2),
+    "rank0-of-64-2micro": SMALL["cfg4-small"].replace(steps=2, micro_steps=2),
+    "halfreduce-bf16-3micro": SMALL["cfg2-small"].replace(steps=2, micro_steps=3,
+                                                          half_reduce=True),
+}
+
+
+@pytest.mark.parametrize("name", list(ACCUM))
+def test_accumulation_lockstep(name):
+    """K micro-steps of zero_reduce_scatter_accumulate, then
+    zero_step_fused_accumulated, against the oracle, step after step; the
+    injected +Inf (in one micro-step) skips that step."""
+    from zs_harness import INF_BITS, gen_master, half_bits
+    wl = ACCUM[name]
+    ls = Lockstep(wl)
+    for s in range(1, wl.steps + 1):
+        S = ls.st.loss_scale
+        n_acc = ls.lay.padded if wl.rank is None else ls.lay.owned
+        acc = np.zeros(n_acc, np.float32)
+        for k in range(wl.micro_steps):
+            grads = gen_grads(wl, ls.lay, s, S)  # step s, then vary per micro-step
+            if k:
+                grads = _micro_grads(wl, ls.lay, s, k, S)
+            ls.z.accumulate([to_dev_half(g, wl.dtype) for g in grads], add=k > 0)
+            oracle.reduce_scatter_accumulate(grads, wl.dtype, ls.lay, acc, k > 0, rank=wl.rank,
+                                             grads_are_slices=wl.grads_are_slices,
+                                             half_reduce=wl.half_reduce)
+        ls.z.step_accumulated()
+        oracle.step_accumulated(acc, wl.dtype, ls.lay, ls.ocfg, ls.st, ls.w, ls.m, ls.v, ls.half,
+                                rank=wl.rank)
+        ls.steps += 1
+        torch.cuda.synchronize()
+        assert np.array_equal(ls.z.acc.cpu().numpy().view(np.uint32), acc.view(np.uint32))
+        ls.check()
+    if name == "flat-nd16-4micro":
+        assert ls.st.skipped == 1
+
+
+def _micro_grads(wl, lay, step, micro, loss_scale):
+    from zs_harness import tensor_mask, rank_index
+    mask = tensor_mask(lay)
+    out = []
+    for q in range(wl.world):
+        g = synth.fill_half(wl.grad_key(step, q, micro), 0, lay.padded,
+                            wl.grad_sigma * loss_scale, wl.dtype)
+        g[~mask] = 0
+        out.append(g)
+    if wl.grads_are_slices:
+        idx = rank_index(lay, wl.rank)
+        out = [g[idx].copy() for g in out]
+    return out
+
+
+def test_one_micro_step_equals_the_fused_step():
+    """Accumulating a single micro-step and stepping from it gives the fused
+    step's bits."""
+    wl = CFG1.replace(numels=(200_003,), world=4, steps=2, inject_at=())
+    a, b = Lockstep(wl), Lockstep(wl)
+    for s in range(1, 3):
+        grads = gen_grads(wl, a.lay, s, a.st.loss_scale)
+        a.step(grads)
+        b.z.accumulate([to_dev_half(g, wl.dtype) for g in grads], add=False)
+        b.z.step_accumulated()
+    torch.cuda.synchronize()
+    for x, y in zip(a.z.current(), b.z.current()):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+# ----------------------------------------------------------------- half-precision reduction
+
+HALFRED = {
+    "fp16-nd16-dynamic": SMALL["cfg3-small"].replace(half_reduce=True),
+    "bf16-nd8-clip": SMALL["cfg2-small"].replace(half_reduce=True, steps=3),
+    "fp16-rank0-of-64-slices": SMALL["cfg4-small"].replace(half_reduce=True),
+    "bucketed-bf16-clip": SMALL["cfg5-small"].replace(half_reduce=True),
+    "three-ranks": EDGE["three-ranks-generic"].replace(half_reduce=True),
+}
+
+
+@pytest.mark.parametrize("name", list(HALFRED))
+def test_half_reduce_lockstep(name):
+    """The reduction in the gradients' own half type (every partial sum
+    rounded to nearest even) against the oracle, step after step."""
+    wl = HALFRED[name]
+    ls = Lockstep(wl)
+    for _ in range(wl.steps):
+        ls.step()
+        ls.check()
+
+
+def test_half_reduce_overflow_skips_where_fp32_does_not():
+    """fp16 gradients near the top of the range: a partial sum overflows in
+    fp16 (the step is skipped) although the fp32 reduction stays finite."""
+    wl = CFG1.replace(numels=(50_000,), world=4, steps=1, inject_at=(), loss_scale=2.0 ** 24,
+                      dynamic_scale=True)
+    fp32, half = Lockstep(wl), Lockstep(wl.replace(half_reduce=True))
+    fp32.step()
+    half.step()
+    a, b = fp32.check(), half.check()
+    assert a.overflow == 0 and a.t == 1
+    assert b.overflow == 1 and b.t == 0 and b.loss_scale == 2.0 ** 23

@@ -127,7 +127,8 @@ class Lockstep:
         rank = -1 if wl.rank is None else wl.rank
         self.z = zs.ZeroStep(wl.numels, wl.world, wl.dtype, self.zcfg, loss_scale=wl.loss_scale,
                              rank=rank, bucket_numel=wl.bucket, align_elems=wl.align,
-                             grads_are_slices=wl.grads_are_slices, stage_grad=stage)
+                             grads_are_slices=wl.grads_are_slices, stage_grad=stage,
+                             half_reduce=wl.half_reduce)
         L = self.z.layout
         assert (L.padded_numel, L.owned_numel) == (self.lay.padded, self.lay.owned)
         master = gen_master(wl, self.lay)
@@ -149,7 +150,8 @@ class Lockstep:
             grads = gen_grads(wl, self.lay, self.steps, self.st.loss_scale)
         self.z.step([to_dev_half(g, wl.dtype) for g in grads])
         oracle.step(grads, wl.dtype, self.lay, self.ocfg, self.st, self.w, self.m, self.v,
-                    self.half, rank=wl.rank, grads_are_slices=wl.grads_are_slices)
+                    self.half, rank=wl.rank, grads_are_slices=wl.grads_are_slices,
+                    half_reduce=wl.half_reduce)
 
     def check(self):
         torch.cuda.synchronize()

@@ -21,11 +21,14 @@ import torch
 
 from ._abi import (BF16, F16, MAX_WORLD, AdamCfg, Layout, StepState, ZeroError, check, lib)
 
+HALF_REDUCE = 2  # added to F16 / BF16: reduce in the half type instead of fp32
+
 __all__ = [
     "F16", "BF16", "MAX_WORLD", "AdamCfg", "Layout", "StepState", "ZeroError", "ZeroStep",
     "adam_cfg", "new_state", "read_state", "state_field_ptr", "zero_partition_layout",
     "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
     "zero_grad_norm", "zero_grad_norm_noalloc", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
+    "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated",
 ]
 
 _TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
@@ -114,12 +117,17 @@ def state_field_ptr(state: torch.Tensor, field: str) -> int:
 
 # ----------------------------------------------------------------- device entry points
 
+def _grad_code(grads, half_reduce: bool) -> int:
+    return _dtype_code(grads[0]) | (HALF_REDUCE if half_reduce else 0)
+
+
 def zero_reduce_scatter_sum(grads: Sequence[torch.Tensor], layout: Layout, g_out: torch.Tensor,
-                            rank: int = -1, grads_are_slices: bool = False, stream=None) -> None:
+                            rank: int = -1, grads_are_slices: bool = False, stream=None,
+                            half_reduce: bool = False) -> None:
     check("zero_reduce_scatter_sum",
           lib().zero_reduce_scatter_sum(_ptr_array(grads), int(grads_are_slices),
-                                        _dtype_code(grads[0]), ctypes.byref(layout), rank,
-                                        _dev_ptr(g_out), _stream(stream)))
+                                        _grad_code(grads, half_reduce), ctypes.byref(layout),
+                                        rank, _dev_ptr(g_out), _stream(stream)))
 
 
 def zero_check_overflow(g: torch.Tensor, inv_scale: float, flag_ptr: int, stream=None) -> None:
@@ -163,15 +171,43 @@ def zero_step_fused(grads: Sequence[torch.Tensor], layout: Layout,
                     v: Sequence[torch.Tensor], params: Sequence[torch.Tensor], cfg: AdamCfg,
                     state: torch.Tensor, ws: torch.Tensor, rank: int = -1,
                     g_stage: Optional[torch.Tensor] = None, grads_are_slices: bool = False,
-                    stream=None) -> None:
+                    stream=None, half_reduce: bool = False) -> None:
     """The whole step (a2)-(a8).  master, m, v and params are the two
     ping-pong slots (the same tensor twice for an in-place clipped step)."""
     check("zero_step_fused",
-          lib().zero_step_fused(_ptr_array(grads), int(grads_are_slices), _dtype_code(grads[0]),
+          lib().zero_step_fused(_ptr_array(grads), int(grads_are_slices),
+                                _grad_code(grads, half_reduce),
                                 ctypes.byref(layout), rank, _ptr_array(master), _ptr_array(m),
                                 _ptr_array(v), _ptr_array(params), _dev_ptr(g_stage),
                                 ctypes.byref(cfg), _dev_ptr(state), _dev_ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def zero_reduce_scatter_accumulate(grads: Sequence[torch.Tensor], layout: Layout,
+                                   acc: torch.Tensor, add: bool, rank: int = -1,
+                                   grads_are_slices: bool = False, stream=None,
+                                   half_reduce: bool = False) -> None:
+    """One micro-step of gradient accumulation: acc = (acc if add else 0) +
+    the reduce-scatter sum of the ranks' half gradients."""
+    check("zero_reduce_scatter_accumulate",
+          lib().zero_reduce_scatter_accumulate(_ptr_array(grads), int(grads_are_slices),
+                                               _grad_code(grads, half_reduce),
+                                               ctypes.byref(layout), rank,
+                                               _dev_ptr(acc), int(add), _stream(stream)))
+
+
+def zero_step_fused_accumulated(acc: torch.Tensor, dtype: int, layout: Layout,
+                                master: Sequence[torch.Tensor], m: Sequence[torch.Tensor],
+                                v: Sequence[torch.Tensor], params: Sequence[torch.Tensor],
+                                cfg: AdamCfg, state: torch.Tensor, ws: torch.Tensor,
+                                rank: int = -1, stream=None) -> None:
+    """The step with the gradient taken from the fp32 accumulator."""
+    check("zero_step_fused_accumulated",
+          lib().zero_step_fused_accumulated(_dev_ptr(acc), dtype, ctypes.byref(layout), rank,
+                                            _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                                            _ptr_array(params), ctypes.byref(cfg),
+                                            _dev_ptr(state), _dev_ptr(ws),
+                                            ws.numel() * ws.element_size(), _stream(stream)))
 
 
 # ----------------------------------------------------------------- buffer owner
@@ -190,9 +226,10 @@ class ZeroStep:
     def __init__(self, numels: Sequence[int], world: int, dtype: int, cfg: AdamCfg,
                  loss_scale: float = 1.0, rank: int = -1, bucket_numel: int = 0,
                  align_elems: int = 64, grads_are_slices: bool = False,
-                 stage_grad: Optional[bool] = None, device="cuda"):
+                 stage_grad: Optional[bool] = None, device="cuda", half_reduce: bool = False):
         self.layout, self.offsets = zero_partition_layout(numels, world, align_elems, bucket_numel)
         self.world, self.dtype, self.cfg, self.rank = world, dtype, cfg, rank
+        self.half_reduce = half_reduce
         self.grads_are_slices = grads_are_slices
         L = self.layout
         self.n_state = L.padded_numel if rank < 0 else L.owned_numel
@@ -233,19 +270,42 @@ class ZeroStep:
     def step(self, grads: Sequence[torch.Tensor], stream=None) -> None:
         zero_step_fused(grads, self.layout, self.master, self.m, self.v, self.params, self.cfg,
                         self.state, self.ws, self.rank, self.g_stage, self.grads_are_slices,
-                        stream)
+                        stream, self.half_reduce)
+
+    def accumulate(self, grads: Sequence[torch.Tensor], add: bool, stream=None) -> None:
+        """One micro-step into the group's fp32 gradient accumulator (allocated
+        on first use); add=False starts a new accumulation."""
+        if getattr(self, "acc", None) is None:
+            self.acc = torch.empty(self.n_state, dtype=torch.float32, device=self.state.device)
+        zero_reduce_scatter_accumulate(grads, self.layout, self.acc, add, self.rank,
+                                       self.grads_are_slices, stream, self.half_reduce)
+
+    def step_accumulated(self, stream=None) -> None:
+        """The step from the accumulated gradient."""
+        zero_step_fused_accumulated(self.acc, self.dtype, self.layout, self.master, self.m,
+                                    self.v, self.params, self.cfg, self.state, self.ws, self.rank,
+                                    stream)
 
     def step_from_host(self, host_grads: Sequence[torch.Tensor],
-                       device_grads: Sequence[torch.Tensor], stream=None) -> StepState:
-        """End to end: copy each rank's gradient from (pinned) host memory,
-        run the step and read the step state back to the host."""
+                       device_grads: Sequence[torch.Tensor], stream=None,
+                       micro_steps: int = 1) -> StepState:
+        """End to end: copy each rank's gradient from (pinned) host memory, run
+        the step and read the step state back to the host.  With
+        micro_steps > 1 the copy is repeated for every micro-step (the same
+        host buffers stand for each) and accumulated before the step."""
         s = stream if stream is not None else torch.cuda.current_stream()
         if getattr(self, "_state_host", None) is None:
             self._state_host = torch.empty(64, dtype=torch.uint8, pin_memory=True)
         with torch.cuda.stream(s):
-            for h, d in zip(host_grads, device_grads):
-                d.copy_(h, non_blocking=True)
-            self.step(device_grads, s)
+            for k in range(micro_steps):
+                for h, d in zip(host_grads, device_grads):
+                    d.copy_(h, non_blocking=True)
+                if micro_steps > 1:
+                    self.accumulate(device_grads, k > 0, s)
+            if micro_steps > 1:
+                self.step_accumulated(s)
+            else:
+                self.step(device_grads, s)
             self._state_host.copy_(self.state, non_blocking=True)
         s.synchronize()
         return StepState.from_buffer_copy(bytes(self._state_host.numpy().tobytes()))

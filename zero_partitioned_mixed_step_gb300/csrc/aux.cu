@@ -309,7 +309,7 @@ int zero_adam_step(const float *g, float *master, float *m, float *v, void *half
     int rc = check_cfg(cfg);
     if (rc)
         return rc;
-    if (n < 0 || !state_dev || (dtype != ZERO_F16 && dtype != ZERO_BF16) ||
+    if (n < 0 || !state_dev || dtype < ZERO_F16 || dtype > ZERO_BF16_HALF_REDUCE ||
         (n > 0 && (!g || !master || !m || !v || !half_out)))
         return ZERO_EINVAL;
     if (!aligned32(g) || !aligned32(master) || !aligned32(m) || !aligned32(v) ||
@@ -320,7 +320,7 @@ int zero_adam_step(const float *g, float *master, float *m, float *v, void *half
     const CfgDev c{cfg->lr, cfg->beta1, cfg->beta2, cfg->eps, cfg->weight_decay,
                    cfg->max_grad_norm, cfg->adamw ? 1 : 0, cfg->bias_correction ? 1 : 0};
     uint16_t *out = static_cast<uint16_t *>(half_out);
-    if (dtype == ZERO_F16) {
+    if (!is_bf16(dtype)) {  // the output's storage type
         const int gx = grid_for(reinterpret_cast<const void *>(adam_kernel<ZERO_F16>), n / kUnit);
         adam_kernel<ZERO_F16><<<gx, kThreads, 0, stream>>>(g, master, m, v, out, n, c, state_dev);
     } else {

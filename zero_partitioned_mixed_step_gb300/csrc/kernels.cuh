@@ -86,6 +86,11 @@ __device__ __forceinline__ float4 ld_state4(const float *p)
 
 // ------------------------------------------------------------------ conversions
 
+// DT is a zero_dtype: bit 0 selects bfloat16 (else binary16), bit 1 a
+// reduction carried out in that type instead of in fp32.
+__host__ __device__ constexpr bool is_bf16(int dt) { return (dt & 1) != 0; }
+__host__ __device__ constexpr bool half_reduce(int dt) { return (dt & 2) != 0; }
+
 // Add the 8 half-precision values of x (exactly converted to fp32) to acc.
 template <int DT>
 __device__ __forceinline__ void add_half8(float acc[8], const uint4 x)
@@ -94,7 +99,7 @@ __device__ __forceinline__ void add_half8(float acc[8], const uint4 x)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float lo, hi;
-        if constexpr (DT == ZERO_F16) {
+        if constexpr (!is_bf16(DT)) {
             __half2 h = *reinterpret_cast<const __half2 *>(&u[j]);
             float2 f = __half22float2(h);
             lo = f.x;
@@ -115,7 +120,7 @@ __device__ __forceinline__ uint4 pack_half8(const float w[8])
     uint32_t u[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if constexpr (DT == ZERO_F16) {
+        if constexpr (!is_bf16(DT)) {
             __half2 h = __floats2half2_rn(w[2 * j], w[2 * j + 1]);
             u[j] = *reinterpret_cast<uint32_t *>(&h);
         } else {
@@ -124,6 +129,26 @@ __device__ __forceinline__ uint4 pack_half8(const float w[8])
         }
     }
     return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+// Half-precision running sums: acc holds 4 packed pairs in the gradient's type;
+// add the 8 values of x with one round-to-nearest-even addition per element.
+template <int DT>
+__device__ __forceinline__ void add_half8_in_half(uint32_t acc[4], const uint4 x)
+{
+    const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (!is_bf16(DT)) {
+            __half2 a = *reinterpret_cast<const __half2 *>(&acc[j]);
+            a = __hadd2(a, *reinterpret_cast<const __half2 *>(&u[j]));
+            acc[j] = *reinterpret_cast<uint32_t *>(&a);
+        } else {
+            __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&acc[j]);
+            a = __hadd2(a, *reinterpret_cast<const __nv_bfloat162 *>(&u[j]));
+            acc[j] = *reinterpret_cast<uint32_t *>(&a);
+        }
+    }
 }
 
 __device__ __forceinline__ bool nonfinite(float x)
@@ -145,6 +170,27 @@ template <int DT, int W, int MAXW>
 __device__ __forceinline__ void reduce_unit(const GradTable<MAXW> &t, int world, int64_t gi,
                                             float acc[8], uint64_t pol)
 {
+    if constexpr (half_reduce(DT)) {
+        // running sums in the half type, from +0, one rounding per addition
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        int q = 0;
+        for (; q + 8 <= world; q += 8) {
+            uint4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                x[j] = ld_stream(t.p[q + j] + gi, pol);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                add_half8_in_half<DT>(h, x[j]);
+        }
+        for (; q < world; ++q)
+            add_half8_in_half<DT>(h, ld_stream(t.p[q] + gi, pol));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[i] = 0.0f;
+        add_half8<DT>(acc, make_uint4(h[0], h[1], h[2], h[3]));  // exact widening
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         acc[i] = 0.0f;
@@ -307,7 +353,7 @@ __device__ __forceinline__ void adam8(const float g[8], float w[8], float m[8], 
 template <int DT>
 __device__ __forceinline__ uint16_t round_half1(float w)
 {
-    if constexpr (DT == ZERO_F16)
+    if constexpr (!is_bf16(DT))
         return __half_as_ushort(__float2half_rn(w));
     else
         return __bfloat16_as_ushort(__float2bfloat16_rn(w));

@@ -13,11 +13,38 @@
 //   PASS2_*    (a5 clip)-(a7) of a clipped step, skipped when pass 1 flagged
 //              an overflow; g is reduced again or read from the stage.
 //   RS         (a2) alone: the reduced fp32 gradient.
+//   RS_ACC     (a2) into an fp32 accumulator (gradient accumulation).
+//   ACC_*      the step with the gradient read from an fp32 accumulator (the
+//              sum of micro-steps' reduced, still scaled gradients) instead of
+//              the N_d half buffers: FUSED, PASS1 and PASS2 as above.
 #include "kernels.cuh"
 
 namespace zs {
 
-enum Mode { M_FUSED = 0, M_PASS1 = 1, M_PASS2_RECOMPUTE = 2, M_PASS2_STAGED = 3, M_RS = 4 };
+enum Mode {
+    M_FUSED = 0, M_PASS1 = 1, M_PASS2_RECOMPUTE = 2, M_PASS2_STAGED = 3, M_RS = 4,
+    M_RS_ACC = 5, M_ACC_FUSED = 6, M_ACC_PASS1 = 7, M_ACC_PASS2 = 8
+};
+
+// What each mode does with a unit.
+__host__ __device__ constexpr bool reads_half_grads(int m)
+{
+    return m == M_FUSED || m == M_PASS1 || m == M_PASS2_RECOMPUTE || m == M_RS || m == M_RS_ACC;
+}
+__host__ __device__ constexpr bool reads_accumulator(int m)
+{
+    return m == M_ACC_FUSED || m == M_ACC_PASS1 || m == M_ACC_PASS2;
+}
+__host__ __device__ constexpr bool flags_overflow(int m)
+{
+    return m == M_FUSED || m == M_PASS1 || m == M_ACC_FUSED || m == M_ACC_PASS1;
+}
+__host__ __device__ constexpr bool sums_squares(int m) { return m == M_PASS1 || m == M_ACC_PASS1; }
+__host__ __device__ constexpr bool second_pass(int m)
+{
+    return m == M_PASS2_RECOMPUTE || m == M_PASS2_STAGED || m == M_ACC_PASS2;
+}
+__host__ __device__ constexpr bool reduces_only(int m) { return m == M_RS || m == M_RS_ACC; }
 
 template <int MAXW>
 struct StepParams {
@@ -28,8 +55,9 @@ struct StepParams {
     const float *w0, *w1, *m0, *m1, *v0, *v1;  // ping-pong slots (reads)
     float *wo0, *wo1, *mo0, *mo1, *vo0, *vo1;   // ping-pong slots (writes)
     uint16_t *par0, *par1;                      // parameter buffer slots
-    float *stage;                               // PASS1 output / PASS2_STAGED input / RS output
-    double *partials;                           // PASS1: one per CTA
+    float *stage;      // PASS1 output / PASS2_STAGED input / RS output / accumulator
+    double *partials;  // PASS1: one per CTA
+    int32_t add;       // RS_ACC: add to the accumulator (else overwrite it)
 };
 
 template <int DT, int W, int MAXW, int MODE, bool ALL>
@@ -40,7 +68,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ int sh_cur;
     Scalars s{};
     int cur = 0;
-    if constexpr (MODE != M_RS) {
+    if constexpr (!reduces_only(MODE)) {
         if (threadIdx.x == 0) {
             compute_scalars(p.cfg, p.state, sh);
             sh_cur = p.state->cur;
@@ -48,7 +76,7 @@ __global__ void __launch_bounds__(kThreads)
         __syncthreads();
         s = sh;
         cur = sh_cur;
-        if constexpr (MODE == M_PASS2_RECOMPUTE || MODE == M_PASS2_STAGED) {
+        if constexpr (second_pass(MODE)) {
             if (s.skip)
                 return;  // the whole step is skipped: write nothing
         }
@@ -71,10 +99,26 @@ __global__ void __launch_bounds__(kThreads)
         locate<ALL>(vw, u, f, si, gi);
         float g[8];
         if constexpr (MODE == M_PASS2_STAGED) {
+            load8(p.stage + si, g);  // already unscaled by pass 1
+        } else if constexpr (reads_accumulator(MODE)) {
             load8(p.stage + si, g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                g[i] = __fmul_rn(g[i], s.inv_s);
         } else {
             reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g, pol);
             if constexpr (MODE == M_RS) {
+                store8(p.stage + si, g);
+                continue;
+            }
+            if constexpr (MODE == M_RS_ACC) {
+                if (p.add) {
+                    float a[8];
+                    load8(p.stage + si, a);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        g[i] = __fadd_rn(a[i], g[i]);
+                }
                 store8(p.stage + si, g);
                 continue;
             }
@@ -82,18 +126,18 @@ __global__ void __launch_bounds__(kThreads)
             for (int i = 0; i < 8; ++i)
                 g[i] = __fmul_rn(g[i], s.inv_s);
         }
-        if constexpr (MODE == M_FUSED || MODE == M_PASS1) {
+        if constexpr (flags_overflow(MODE)) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 bad |= nonfinite(g[i]);
         }
-        if constexpr (MODE == M_PASS1) {
+        if constexpr (sums_squares(MODE)) {
             ss.add8(g);
-            if (p.stage)
+            if (MODE == M_PASS1 && p.stage)
                 store8(p.stage + si, g);
             continue;
         }
-        if constexpr (MODE == M_PASS2_RECOMPUTE || MODE == M_PASS2_STAGED) {
+        if constexpr (second_pass(MODE)) {
             if (s.coef < 1.0f) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -110,9 +154,9 @@ __global__ void __launch_bounds__(kThreads)
         store8(v_dst + si, v);
         st_half8(out + f, pack_half8<DT>(w), pol);
     }
-    if constexpr (MODE == M_FUSED || MODE == M_PASS1)
+    if constexpr (flags_overflow(MODE))
         flag_nonfinite(bad, &p.state->found_inf);
-    if constexpr (MODE == M_PASS1) {
+    if constexpr (sums_squares(MODE)) {
         const double tot = block_sum(ss.acc);
         if (threadIdx.x == 0)
             p.partials[blockIdx.x] = tot;
@@ -139,7 +183,9 @@ int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
 template <int DT, int MAXW, int MODE>
 int dispatch_world(const StepParams<MAXW> &p, cudaStream_t stream, int *gx)
 {
-    if constexpr (MODE == M_PASS2_STAGED) {
+    if constexpr (!reads_half_grads(MODE) || half_reduce(DT)) {
+        // no gradient loads, or the half-precision reduction: one instance
+        // with the group size read at run time
         return launch_one<DT, 0, MAXW, MODE>(p, stream, gx);
     } else if constexpr (MAXW == 64) {
         switch (p.view.world) {
@@ -159,22 +205,38 @@ int dispatch_world(const StepParams<MAXW> &p, cudaStream_t stream, int *gx)
 template <int MAXW>
 int dispatch(const StepParams<MAXW> &p, zero_dtype dt, int mode, cudaStream_t s, int *gx)
 {
-#define ZS_MODES(DT)                                                      \
-    switch (mode) {                                                       \
-    case M_FUSED: return dispatch_world<DT, MAXW, M_FUSED>(p, s, gx); \
-    case M_PASS1: return dispatch_world<DT, MAXW, M_PASS1>(p, s, gx); \
-    case M_PASS2_RECOMPUTE:                                               \
-        return dispatch_world<DT, MAXW, M_PASS2_RECOMPUTE>(p, s, gx); \
-    case M_PASS2_STAGED:                                                  \
-        return dispatch_world<DT, MAXW, M_PASS2_STAGED>(p, s, gx); \
-    default: return dispatch_world<DT, MAXW, M_RS>(p, s, gx);     \
+#define ZS_MODES(DT)                                                              \
+    switch (mode) {                                                               \
+    case M_FUSED: return dispatch_world<DT, MAXW, M_FUSED>(p, s, gx);             \
+    case M_PASS1: return dispatch_world<DT, MAXW, M_PASS1>(p, s, gx);             \
+    case M_PASS2_RECOMPUTE: return dispatch_world<DT, MAXW, M_PASS2_RECOMPUTE>(p, s, gx); \
+    case M_RS_ACC: return dispatch_world<DT, MAXW, M_RS_ACC>(p, s, gx);           \
+    default: return dispatch_world<DT, MAXW, M_RS>(p, s, gx);                     \
     }
-    if (dt == ZERO_F16) {
-        ZS_MODES(ZERO_F16)
-    } else {
-        ZS_MODES(ZERO_BF16)
+#define ZS_NO_GRAD_MODES(DT)                                                      \
+    switch (mode) {                                                               \
+    case M_PASS2_STAGED: return dispatch_world<DT, MAXW, M_PASS2_STAGED>(p, s, gx); \
+    case M_ACC_FUSED: return dispatch_world<DT, MAXW, M_ACC_FUSED>(p, s, gx);     \
+    case M_ACC_PASS1: return dispatch_world<DT, MAXW, M_ACC_PASS1>(p, s, gx);     \
+    default: return dispatch_world<DT, MAXW, M_ACC_PASS2>(p, s, gx);              \
+    }
+    const bool grads = mode == M_FUSED || mode == M_PASS1 || mode == M_PASS2_RECOMPUTE ||
+                       mode == M_RS || mode == M_RS_ACC;
+    if (!grads) {  // only the parameters' storage type matters
+        if (is_bf16(dt)) {
+            ZS_NO_GRAD_MODES(ZERO_BF16)
+        } else {
+            ZS_NO_GRAD_MODES(ZERO_F16)
+        }
+    }
+    switch (dt) {
+    case ZERO_F16: ZS_MODES(ZERO_F16)
+    case ZERO_BF16: ZS_MODES(ZERO_BF16)
+    case ZERO_F16_HALF_REDUCE: ZS_MODES(ZERO_F16_HALF_REDUCE)
+    default: ZS_MODES(ZERO_BF16_HALF_REDUCE)
     }
 #undef ZS_MODES
+#undef ZS_NO_GRAD_MODES
 }
 
 // Everything a pass needs besides the per-mode pointers.
@@ -190,6 +252,7 @@ struct PassArgs {
     void *const *params;
     float *stage;
     double *partials;
+    int add;
 };
 
 template <int MAXW>
@@ -232,6 +295,7 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
     }
     p.stage = a.stage;
     p.partials = a.partials;
+    p.add = a.add;
     return dispatch<MAXW>(p, a.dtype, mode, stream, gx);
 }
 
@@ -248,7 +312,8 @@ int check_grads(const void *const *grads, int grads_are_slices, zero_dtype dtype
     int rc = check_layout(lay);
     if (rc)
         return rc;
-    if (!grads || (dtype != ZERO_F16 && dtype != ZERO_BF16) || rank < -1 || rank >= lay->world ||
+    if (!grads || dtype < ZERO_F16 || dtype > ZERO_BF16_HALF_REDUCE || rank < -1 ||
+        rank >= lay->world ||
         (grads_are_slices && rank < 0))
         return ZERO_EINVAL;
     for (int q = 0; q < lay->world; ++q) {
@@ -258,6 +323,57 @@ int check_grads(const void *const *grads, int grads_are_slices, zero_dtype dtype
             return ZERO_EALIGN;
     }
     return ZERO_OK;
+}
+
+// Checks of the ping-pong slots, stage, state and workspace shared by the
+// fused entry points.
+int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *const master[2],
+                float *const m[2], float *const v[2], void *const params[2], const float *stage,
+                bool stage_allowed, const zero_step_state *state_dev, const void *ws,
+                size_t ws_bytes)
+{
+    if (!master || !m || !v || !params || !state_dev || !ws)
+        return ZERO_EINVAL;
+    const bool clip = cfg->max_grad_norm > 0.0;
+    const bool empty = layout->padded_numel == 0;  // nothing to read or write
+    for (int s = 0; s < 2; ++s) {
+        if (!empty && (!master[s] || !m[s] || !v[s] || !params[s]))
+            return ZERO_EINVAL;
+        if (!aligned32(master[s]) || !aligned32(m[s]) || !aligned32(v[s]) || !aligned16(params[s]))
+            return ZERO_EALIGN;
+    }
+    if (!clip && !empty &&
+        (master[0] == master[1] || m[0] == m[1] || v[0] == v[1] || params[0] == params[1]))
+        return ZERO_EINVAL;  // a one-pass step needs distinct slots to be able to skip
+    if (stage && !stage_allowed)
+        return ZERO_EINVAL;
+    if ((stage && !aligned32(stage)) || !aligned16(ws) ||
+        (reinterpret_cast<uintptr_t>(state_dev) & 7u))
+        return ZERO_EALIGN;
+    if (ws_bytes < zero_workspace_bytes(layout->world))
+        return ZERO_ESPACE;
+    return ZERO_OK;
+}
+
+// One step (one or two passes, then the finalize) in the given modes.
+int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream)
+{
+    int rc, gx = 1;
+    if (a.lay->padded_numel > 0) {
+        if (!clip) {
+            if ((rc = run(a, one_pass, stream, &gx)))
+                return rc;
+        } else {
+            if ((rc = run(a, pass1, stream, &gx)))
+                return rc;
+            if ((rc = launch_norm_finalize(a.partials, gx, 1, a.cfg->max_grad_norm, a.state,
+                                           nullptr, stream)))
+                return rc;
+            if ((rc = run(a, pass2, stream, &gx)))
+                return rc;
+        }
+    }
+    return launch_finalize(a.cfg, a.state, 1, stream);
 }
 
 }  // namespace zs
@@ -278,9 +394,28 @@ extern "C" int zero_reduce_scatter_sum(const void *const *grads, int grads_are_s
     if (layout->padded_numel == 0)
         return ZERO_OK;
     PassArgs a{grads, grads_are_slices, dtype, layout, rank, nullptr, nullptr,
-               nullptr, nullptr, nullptr, nullptr, g_out, nullptr};
+               nullptr, nullptr, nullptr, nullptr, g_out, nullptr, 0};
     int gx;
     return run(a, M_RS, stream, &gx);
+}
+
+extern "C" int zero_reduce_scatter_accumulate(const void *const *grads, int grads_are_slices,
+                                              zero_dtype dtype, const zero_layout *layout,
+                                              int rank, float *acc, int add, zero_stream_t stream)
+{
+    int rc = check_grads(grads, grads_are_slices, dtype, layout, rank);
+    if (rc)
+        return rc;
+    if (!acc && layout->padded_numel)
+        return ZERO_EINVAL;
+    if (!aligned32(acc))
+        return ZERO_EALIGN;
+    if (layout->padded_numel == 0)
+        return ZERO_OK;
+    PassArgs a{grads, grads_are_slices, dtype, layout, rank, nullptr, nullptr,
+               nullptr, nullptr, nullptr, nullptr, acc, nullptr, add ? 1 : 0};
+    int gx;
+    return run(a, M_RS_ACC, stream, &gx);
 }
 
 extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, zero_dtype dtype,
@@ -295,44 +430,40 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
         return rc;
     if ((rc = check_cfg(cfg)))
         return rc;
-    if (!master || !m || !v || !params || !state_dev || !ws)
-        return ZERO_EINVAL;
     const bool clip = cfg->max_grad_norm > 0.0;
-    const bool empty = layout->padded_numel == 0;  // nothing to read or write
-    for (int s = 0; s < 2; ++s) {
-        if (!empty && (!master[s] || !m[s] || !v[s] || !params[s]))
-            return ZERO_EINVAL;
-        if (!aligned32(master[s]) || !aligned32(m[s]) || !aligned32(v[s]) || !aligned16(params[s]))
-            return ZERO_EALIGN;
-    }
-    if (!clip && !empty &&
-        (master[0] == master[1] || m[0] == m[1] || v[0] == v[1] || params[0] == params[1]))
-        return ZERO_EINVAL;  // a one-pass step needs distinct slots to be able to skip
-    if (g_stage && !clip)
-        return ZERO_EINVAL;
-    if ((g_stage && !aligned32(g_stage)) || !aligned16(ws) ||
-        (reinterpret_cast<uintptr_t>(state_dev) & 7u))
-        return ZERO_EALIGN;
-    if (ws_bytes < zero_workspace_bytes(layout->world))
-        return ZERO_ESPACE;
-
+    if ((rc = check_slots(layout, cfg, master, m, v, params, g_stage, clip, state_dev, ws,
+                          ws_bytes)))
+        return rc;
     double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
     PassArgs a{grads, grads_are_slices, dtype, layout, rank, cfg, state_dev,
-               master, m, v, params, g_stage, partials};
-    int gx = 1;
-    if (layout->padded_numel > 0) {
-        if (!clip) {
-            if ((rc = run(a, M_FUSED, stream, &gx)))
-                return rc;
-        } else {
-            if ((rc = run(a, M_PASS1, stream, &gx)))
-                return rc;
-            if ((rc = launch_norm_finalize(partials, gx, 1, cfg->max_grad_norm, state_dev,
-                                           nullptr, stream)))
-                return rc;
-            if ((rc = run(a, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE, stream, &gx)))
-                return rc;
-        }
-    }
-    return launch_finalize(cfg, state_dev, 1, stream);
+               master, m, v, params, g_stage, partials, 0};
+    return run_step(a, clip, M_FUSED, M_PASS1, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE,
+                    stream);
+}
+
+extern "C" int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
+                                           const zero_layout *layout, int rank,
+                                           float *const master[2], float *const m[2],
+                                           float *const v[2], void *const params[2],
+                                           const zero_adam_cfg *cfg, zero_step_state *state_dev,
+                                           void *ws, size_t ws_bytes, zero_stream_t stream)
+{
+    int rc = check_layout(layout);
+    if (rc)
+        return rc;
+    if (dtype < ZERO_F16 || dtype > ZERO_BF16_HALF_REDUCE || rank < -1 ||
+        rank >= layout->world || (!acc && layout->padded_numel))
+        return ZERO_EINVAL;
+    if (!aligned32(acc))
+        return ZERO_EALIGN;
+    if ((rc = check_cfg(cfg)))
+        return rc;
+    const bool clip = cfg->max_grad_norm > 0.0;
+    if ((rc = check_slots(layout, cfg, master, m, v, params, nullptr, false, state_dev, ws,
+                          ws_bytes)))
+        return rc;
+    double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
+    PassArgs a{nullptr, 0, dtype, layout, rank, cfg, state_dev,
+               master, m, v, params, const_cast<float *>(acc), partials, 0};
+    return run_step(a, clip, M_ACC_FUSED, M_ACC_PASS1, M_ACC_PASS2, stream);
 }
