@@ -170,7 +170,7 @@ def make_group(wl, device):
     rank = -1 if wl.rank is None else wl.rank
     z = zs.ZeroStep(wl.numels, wl.world, wl.dtype, lib_cfg(wl), loss_scale=wl.loss_scale,
                     rank=rank, bucket_numel=wl.bucket, grads_are_slices=wl.grads_are_slices,
-                    device=device)
+                    device=device, half_reduce=wl.half_reduce, offload_state=wl.offload_state)
     L = z.layout
     gaps = synth.gaps(z.offsets, wl.numels, L.padded_numel)
     segs = [(0, L.padded_numel)] if rank < 0 else z.segments(rank)
@@ -185,10 +185,15 @@ def make_group(wl, device):
                     out[pos + lo - fs:pos + hi - fs].zero_()
             pos += ln
 
-    fill_by_flat(z.master[0], lambda o, fs: synth.gpu_fill_f32(wl.master_key(), fs, o,
-                                                               wl.master_sigma))
+    master0 = z.master[0] if z.master[0].is_cuda else torch.empty(
+        z.master[0].numel(), dtype=torch.float32, device=device)
+    fill_by_flat(master0, lambda o, fs: synth.gpu_fill_f32(wl.master_key(), fs, o,
+                                                           wl.master_sigma))
     if rank < 0:
-        synth.gpu_round_half(z.master[0], z.params[0], wl.dtype)
+        synth.gpu_round_half(master0, z.params[0], wl.dtype)
+    if master0 is not z.master[0]:  # offloaded state: copy the weights to host memory
+        z.master[0].copy_(master0)
+        del master0
     hdt = zs.torch_dtype(wl.dtype)
     grads = []
     sigma = wl.grad_sigma * wl.loss_scale
@@ -435,6 +440,10 @@ def run_ours(args, wl):
                          "sample": desc},
         "e2e": e2e,
         "gpu_launches": launches_per_step * nsteps,
+        **({"host_link": {"bytes_per_step": n_elems * 24,
+                          "gbs": n_elems * 24 / (kernel_ms / 1e3) / 1e9,
+                          "note": "master/m/v read and written in Grace memory over NVLink-C2C"}}
+           if wl.offload_state else {}),
         "clocks": clocks.summary(),
     }
     print(json.dumps(line))

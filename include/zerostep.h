@@ -339,6 +339,14 @@ int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int
  *    reducing it twice (2 * N_d bytes read per element are replaced by 8).
  *  state_dev: device step state.  ws: device workspace of ws_bytes >=
  *    zero_workspace_bytes(layout->world).
+ * Offload (next row f4): master, m and v (all six slots) may instead be
+ *  pinned host memory (cudaHostAlloc / cudaHostRegister) that the GPU reads
+ *  and writes over the host link while gradients and parameters stay in
+ *  device memory, as in ZeRO-Offload, where the optimizer state lives in CPU
+ *  memory ("千亿参数模型如何塞进有限显卡…", "ZeRO-Offload：利用CPU内存"; "DeepSpeed
+ *  ZeRO", "配置说明": offload_optimizer.device = cpu).  The residence is
+ *  detected per call (cudaPointerGetAttributes); mixed residence, or
+ *  offloaded state together with the clip, is ZERO_EINVAL.
  * Pages: all of the above; the ping-pong slots are this library's way to
  * skip a step bit-exactly without a second pass over the gradients.
  */

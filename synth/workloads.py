@@ -75,6 +75,7 @@ class Workload:
     inject_at: Tuple[Tuple[int, int, int], ...] = ()   # (step, rank, flat index)
     micro_steps: int = 1                 # gradient-accumulation micro-steps per step
     half_reduce: bool = False            # reduce in the gradients' half type, not fp32
+    offload_state: bool = False          # master/m/v in pinned host memory
 
     @property
     def numel(self) -> int:
@@ -147,4 +148,9 @@ ACCUM_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-accum4", micro_steps=4, step
 # rounded to fp16), as a half-precision reduce-scatter would produce it.
 HALFRED_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-halfreduce", half_reduce=True)
 
-BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, ACCUM_CFG3, HALFRED_CFG3)}
+# ZeRO-Offload style: the 1.5B, 16-rank workload with the fp32 master weights
+# and moments in Grace memory, reached by the GPU over NVLink-C2C.
+OFFLOAD_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-offload", offload_state=True, steps=10,
+                            inject_every=0)
+
+BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, ACCUM_CFG3, HALFRED_CFG3, OFFLOAD_CFG3)}

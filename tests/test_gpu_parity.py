@@ -388,3 +388,37 @@ def test_half_reduce_overflow_skips_where_fp32_does_not():
     a, b = fp32.check(), half.check()
     assert a.overflow == 0 and a.t == 1
     assert b.overflow == 1 and b.t == 0 and b.loss_scale == 2.0 ** 23
+
+
+# ----------------------------------------------------------------- offloaded optimizer state
+
+OFFLOAD = {
+    "fp16-nd16-dynamic": SMALL["cfg3-small"].replace(offload_state=True),
+    "bf16-rank0-of-64-slices": SMALL["cfg4-small"].replace(offload_state=True,
+                                                           dtype=synth.BF16),
+    "bucketed-rank-view": EDGE["bucketed-rank-slices"].replace(offload_state=True),
+    "fp16-halfreduce": CFG1.replace(numels=(300_003,), world=8, offload_state=True,
+                                    half_reduce=True, inject_at=((2, 7, 123),)),
+}
+
+
+@pytest.mark.parametrize("name", list(OFFLOAD))
+def test_offloaded_state_lockstep(name):
+    """The one-pass step with master, m and v in pinned host memory (read and
+    written by the GPU over the host link) against the oracle."""
+    wl = OFFLOAD[name]
+    ls = Lockstep(wl)
+    assert ls.z.master[0].is_pinned() and not ls.z.master[0].is_cuda
+    for _ in range(wl.steps):
+        ls.step()
+        ls.check()
+
+
+def test_mixed_residence_is_rejected():
+    cfg = zs.adam_cfg()
+    z = zs.ZeroStep((1000,), 2, synth.F16, cfg)
+    grads = [torch.zeros(z.grad_numel(), dtype=torch.float16, device="cuda")] * 2
+    host = torch.zeros_like(z.master[1], device="cpu").pin_memory()
+    with pytest.raises(zs.ZeroError):
+        zs.zero_step_fused(grads, z.layout, [z.master[0], host], z.m, z.v, z.params, cfg,
+                           z.state, z.ws)

@@ -128,7 +128,7 @@ class Lockstep:
         self.z = zs.ZeroStep(wl.numels, wl.world, wl.dtype, self.zcfg, loss_scale=wl.loss_scale,
                              rank=rank, bucket_numel=wl.bucket, align_elems=wl.align,
                              grads_are_slices=wl.grads_are_slices, stage_grad=stage,
-                             half_reduce=wl.half_reduce)
+                             half_reduce=wl.half_reduce, offload_state=wl.offload_state)
         L = self.z.layout
         assert (L.padded_numel, L.owned_numel) == (self.lay.padded, self.lay.owned)
         master = gen_master(wl, self.lay)

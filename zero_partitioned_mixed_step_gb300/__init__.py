@@ -58,6 +58,17 @@ def _ptr_array(tensors: Sequence[torch.Tensor]):
     return (ctypes.c_void_p * len(tensors))(*[_dev_ptr(t) for t in tensors])
 
 
+def _state_ptr(t: torch.Tensor) -> int:
+    """A device tensor, or a pinned host tensor (offloaded optimizer state)."""
+    if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+        raise ValueError("contiguous CUDA or pinned host tensor expected")
+    return t.data_ptr()
+
+
+def _state_array(tensors: Sequence[torch.Tensor]):
+    return (ctypes.c_void_p * len(tensors))(*[_state_ptr(t) for t in tensors])
+
+
 def _stream(stream) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -173,12 +184,13 @@ def zero_step_fused(grads: Sequence[torch.Tensor], layout: Layout,
                     g_stage: Optional[torch.Tensor] = None, grads_are_slices: bool = False,
                     stream=None, half_reduce: bool = False) -> None:
     """The whole step (a2)-(a8).  master, m, v and params are the two
-    ping-pong slots (the same tensor twice for an in-place clipped step)."""
+    ping-pong slots (the same tensor twice for an in-place clipped step);
+    master, m and v may be pinned host tensors (offloaded state)."""
     check("zero_step_fused",
           lib().zero_step_fused(_ptr_array(grads), int(grads_are_slices),
                                 _grad_code(grads, half_reduce),
-                                ctypes.byref(layout), rank, _ptr_array(master), _ptr_array(m),
-                                _ptr_array(v), _ptr_array(params), _dev_ptr(g_stage),
+                                ctypes.byref(layout), rank, _state_array(master), _state_array(m),
+                                _state_array(v), _ptr_array(params), _dev_ptr(g_stage),
                                 ctypes.byref(cfg), _dev_ptr(state), _dev_ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -221,12 +233,15 @@ class ZeroStep:
     double-buffered so an overflow step can be skipped in one pass; with
     clipping they are updated in place and the reduced gradient is staged in
     fp32 between the two passes when that reads fewer bytes (N_d > 4).
+    offload_state keeps master, m and v in pinned host memory (ZeRO-Offload
+    style; the GPU reaches them over the host link).
     """
 
     def __init__(self, numels: Sequence[int], world: int, dtype: int, cfg: AdamCfg,
                  loss_scale: float = 1.0, rank: int = -1, bucket_numel: int = 0,
                  align_elems: int = 64, grads_are_slices: bool = False,
-                 stage_grad: Optional[bool] = None, device="cuda", half_reduce: bool = False):
+                 stage_grad: Optional[bool] = None, device="cuda", half_reduce: bool = False,
+                 offload_state: bool = False):
         self.layout, self.offsets = zero_partition_layout(numels, world, align_elems, bucket_numel)
         self.world, self.dtype, self.cfg, self.rank = world, dtype, cfg, rank
         self.half_reduce = half_reduce
@@ -235,11 +250,14 @@ class ZeroStep:
         self.n_state = L.padded_numel if rank < 0 else L.owned_numel
         clip = cfg.max_grad_norm > 0
         hdt = torch_dtype(dtype)
+        if offload_state and clip:
+            raise ValueError("offloaded optimizer state supports the one-pass step (no clip)")
         f32 = dict(dtype=torch.float32, device=device)
+        st32 = dict(dtype=torch.float32, pin_memory=True) if offload_state else f32
         slots = 1 if clip else 2
-        self.master = [torch.zeros(self.n_state, **f32) for _ in range(slots)]
-        self.m = [torch.zeros(self.n_state, **f32) for _ in range(slots)]
-        self.v = [torch.zeros(self.n_state, **f32) for _ in range(slots)]
+        self.master = [torch.zeros(self.n_state, **st32) for _ in range(slots)]
+        self.m = [torch.zeros(self.n_state, **st32) for _ in range(slots)]
+        self.v = [torch.zeros(self.n_state, **st32) for _ in range(slots)]
         self.params = [torch.zeros(L.padded_numel, dtype=hdt, device=device) for _ in range(slots)]
         if slots == 1:
             for lst in (self.master, self.m, self.v, self.params):

@@ -69,6 +69,22 @@ __device__ __forceinline__ void store8(float *p, const float x[8])
         : "memory");
 }
 
+// The same 8 fp32 values in pinned host memory, reached over the host link:
+// two ordinary 16-byte accesses (zero-copy), evict-first in L2.
+__device__ __forceinline__ void load8_host(const float *p, float x[8])
+{
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(p + 4));
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void store8_host(float *p, const float x[8])
+{
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(x[0], x[1], x[2], x[3]));
+    __stcs(reinterpret_cast<float4 *>(p + 4), make_float4(x[4], x[5], x[6], x[7]));
+}
+
 // 16 bytes of half-precision parameters.
 __device__ __forceinline__ void st_half8(uint16_t *p, uint4 v, uint64_t pol)
 {

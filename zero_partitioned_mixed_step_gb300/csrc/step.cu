@@ -60,7 +60,8 @@ struct StepParams {
     int32_t add;       // RS_ACC: add to the accumulator (else overwrite it)
 };
 
-template <int DT, int W, int MAXW, int MODE, bool ALL>
+// HOST_STATE: master, m and v live in pinned host memory (offload).
+template <int DT, int W, int MAXW, int MODE, bool ALL, bool HOST_STATE = false>
 __global__ void __launch_bounds__(kThreads)
     step_kernel(const __grid_constant__ StepParams<MAXW> p)
 {
@@ -145,13 +146,25 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
         float w[8], m[8], v[8];
-        load8(w_src + si, w);
-        load8(m_src + si, m);
-        load8(v_src + si, v);
+        if constexpr (HOST_STATE) {
+            load8_host(w_src + si, w);
+            load8_host(m_src + si, m);
+            load8_host(v_src + si, v);
+        } else {
+            load8(w_src + si, w);
+            load8(m_src + si, m);
+            load8(v_src + si, v);
+        }
         adam8(g, w, m, v, s);
-        store8(w_dst + si, w);
-        store8(m_dst + si, m);
-        store8(v_dst + si, v);
+        if constexpr (HOST_STATE) {
+            store8_host(w_dst + si, w);
+            store8_host(m_dst + si, m);
+            store8_host(v_dst + si, v);
+        } else {
+            store8(w_dst + si, w);
+            store8(m_dst + si, m);
+            store8(v_dst + si, v);
+        }
         st_half8(out + f, pack_half8<DT>(w), pol);
     }
     if constexpr (flags_overflow(MODE))
@@ -165,11 +178,11 @@ __global__ void __launch_bounds__(kThreads)
 
 // ------------------------------------------------------------------ launch
 
-template <int DT, int W, int MAXW, int MODE>
+template <int DT, int W, int MAXW, int MODE, bool HOST_STATE = false>
 int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
 {
-    auto kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true>
-                                 : step_kernel<DT, W, MAXW, MODE, false>;
+    auto kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true, HOST_STATE>
+                                 : step_kernel<DT, W, MAXW, MODE, false, HOST_STATE>;
     const int target = target_ctas(reinterpret_cast<const void *>(kern));
     const int64_t want = (p.view.units + kThreads - 1) / kThreads;
     const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
@@ -253,7 +266,22 @@ struct PassArgs {
     float *stage;
     double *partials;
     int add;
+    bool host_state = false;  // master/m/v in pinned host memory (one-pass step only)
 };
+
+// The one-pass step with the optimizer state in pinned host memory: one
+// instance per storage type, group size read at run time.
+template <int MAXW>
+int dispatch_host_state(const StepParams<MAXW> &p, zero_dtype dt, cudaStream_t s, int *gx)
+{
+    switch (dt) {
+    case ZERO_F16: return launch_one<ZERO_F16, 0, MAXW, M_FUSED, true>(p, s, gx);
+    case ZERO_BF16: return launch_one<ZERO_BF16, 0, MAXW, M_FUSED, true>(p, s, gx);
+    case ZERO_F16_HALF_REDUCE:
+        return launch_one<ZERO_F16_HALF_REDUCE, 0, MAXW, M_FUSED, true>(p, s, gx);
+    default: return launch_one<ZERO_BF16_HALF_REDUCE, 0, MAXW, M_FUSED, true>(p, s, gx);
+    }
+}
 
 template <int MAXW>
 int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
@@ -296,6 +324,8 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
     p.stage = a.stage;
     p.partials = a.partials;
     p.add = a.add;
+    if (a.host_state)
+        return dispatch_host_state<MAXW>(p, a.dtype, stream, gx);
     return dispatch<MAXW>(p, a.dtype, mode, stream, gx);
 }
 
@@ -323,6 +353,32 @@ int check_grads(const void *const *grads, int grads_are_slices, zero_dtype dtype
             return ZERO_EALIGN;
     }
     return ZERO_OK;
+}
+
+// Where a buffer lives: 1 pinned host memory, 0 device memory, -1 neither
+// (pageable host memory or an unknown pointer).
+int residence(const void *p)
+{
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
+        return 0;
+    return attr.type == cudaMemoryTypeHost ? 1 : -1;
+}
+
+// 1 when all six master/m/v slots are pinned host memory (offload), 0 when
+// all are device memory, ZERO_EINVAL otherwise.
+int state_residence(float *const master[2], float *const m[2], float *const v[2])
+{
+    const void *ptrs[6] = {master[0], master[1], m[0], m[1], v[0], v[1]};
+    int first = residence(ptrs[0]);
+    for (int i = 1; i < 6; ++i)
+        if (residence(ptrs[i]) != first)
+            return ZERO_EINVAL;
+    return first < 0 ? ZERO_EINVAL : first;
 }
 
 // Checks of the ping-pong slots, stage, state and workspace shared by the
@@ -437,6 +493,12 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
     double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
     PassArgs a{grads, grads_are_slices, dtype, layout, rank, cfg, state_dev,
                master, m, v, params, g_stage, partials, 0};
+    if (layout->padded_numel > 0) {
+        const int where = state_residence(master, m, v);
+        if (where < 0 || (where == 1 && clip))
+            return ZERO_EINVAL;  // mixed residence, or offloaded state with the clip
+        a.host_state = where == 1;
+    }
     return run_step(a, clip, M_FUSED, M_PASS1, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE,
                     stream);
 }
