@@ -53,7 +53,7 @@ def algorithmic_bytes_per_elem(world: int, clip: bool, staged: bool, micro: int 
     return b
 
 
-STEP_KERNEL_SOURCES = ("step.cu", "kernels.cuh", "internal.h")
+STEP_KERNEL_SOURCES = ("step.cu", "kernels.cuh", "internal.h", "staged.cuh")
 
 
 def kernel_source_hash(read=None) -> str:

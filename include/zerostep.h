@@ -161,7 +161,8 @@ typedef struct {
     int32_t found_inf;  /* OR of the non-finite flags of the step in progress */
     int32_t cur;        /* ping-pong slot (0/1) holding the current master/m/v/params */
     int32_t skipped;    /* number of skipped steps */
-    int32_t reserved;
+    int32_t error;      /* nonzero if a kernel gave up waiting for its own memory copies
+                           (never expected; that step was skipped); 0 at init */
 } zero_step_state;
 
 /* Human-readable text for a return code (static storage). */

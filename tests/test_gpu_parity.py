@@ -422,3 +422,34 @@ def test_mixed_residence_is_rejected():
     with pytest.raises(zs.ZeroError):
         zs.zero_step_fused(grads, z.layout, [z.master[0], host], z.m, z.v, z.params, cfg,
                            z.state, z.ws)
+
+
+# ----------------------------------------------------------------- staged (TMA bulk-copy) path
+
+@pytest.mark.parametrize("world,dtype", [(1, synth.F16), (2, synth.BF16), (3, synth.F16),
+                                         (8, synth.BF16), (16, synth.F16)])
+def test_staged_path_matches_register_path(world, dtype):
+    """An every-rank one-pass step (the shared-memory staged kernel for
+    N_d <= 16) equals, bit for bit, the same step run rank by rank (the
+    register kernel of one-rank views), over a ragged vector and a skipped
+    step."""
+    wl = CFG1.replace(numels=(777_777, 4097, 3), world=world, dtype=dtype, steps=3,
+                      inject_at=((2, world - 1, 5000),), dynamic_scale=True)
+    full = Lockstep(wl)
+    parts = [Lockstep(wl.replace(rank=r)) for r in range(world)]
+    for s in range(1, wl.steps + 1):
+        grads = gen_grads(wl, full.lay, s, full.st.loss_scale)
+        full.step(grads)
+        for ls in parts:
+            ls.step(grads)
+    full.check()
+    fw, fm, fv, fp = full.z.current()
+    pb = half_bits(fp)
+    for r, ls in enumerate(parts):
+        ls.check()
+        idx = torch.from_numpy(rank_index(full.lay, r)).cuda()
+        w, m, v, p = ls.z.current()
+        assert torch.equal(fw[idx].view(torch.int32), w.view(torch.int32))
+        assert torch.equal(fm[idx].view(torch.int32), m.view(torch.int32))
+        assert torch.equal(fv[idx].view(torch.int32), v.view(torch.int32))
+        assert np.array_equal(pb[idx.cpu().numpy()], half_bits(p)[idx.cpu().numpy()])

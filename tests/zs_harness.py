@@ -161,7 +161,7 @@ class Lockstep:
         assert zs_.t == st.t and zs_.skipped == st.skipped
         assert zs_.beta1_pow == st.bp1 and zs_.beta2_pow == st.bp2
         assert zs_.loss_scale == st.loss_scale and zs_.good_steps == st.good_steps
-        assert zs_.found_inf == 0
+        assert zs_.found_inf == 0 and zs_.error == 0
         if self.ocfg.max_grad_norm > 0 and st.t > 0:
             assert abs(zs_.sumsq - st.sumsq) <= SUMSQ_RTOL * st.sumsq, (zs_.sumsq, st.sumsq)
             assert abs(zs_.clip_coef - st.coef) <= 2.0 ** -23 * st.coef, (zs_.clip_coef, st.coef)

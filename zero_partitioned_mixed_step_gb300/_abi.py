@@ -41,7 +41,7 @@ class StepState(ctypes.Structure):
                 ("loss_scale", ctypes.c_float), ("clip_coef", ctypes.c_float),
                 ("good_steps", ctypes.c_int32), ("overflow", ctypes.c_int32),
                 ("found_inf", ctypes.c_int32), ("cur", ctypes.c_int32),
-                ("skipped", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("skipped", ctypes.c_int32), ("error", ctypes.c_int32)]
 
 
 assert ctypes.sizeof(StepState) == 64

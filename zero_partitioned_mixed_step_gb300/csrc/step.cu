@@ -18,6 +18,7 @@
 //              sum of micro-steps' reduced, still scaled gradients) instead of
 //              the N_d half buffers: FUSED, PASS1 and PASS2 as above.
 #include "kernels.cuh"
+#include "staged.cuh"
 
 namespace zs {
 
@@ -411,13 +412,80 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
     return ZERO_OK;
 }
 
+// The staged one-pass step (staged.cuh), when it applies: every rank at once,
+// fp32 reduction, device-resident state, N_d <= 16.  Returns 1 when it does
+// not apply (the caller then uses the register path).
+template <int DT>
+int launch_staged_dt(const StagedParams &p, cudaStream_t stream)
+{
+    static const int resident = [] {
+        if (cudaFuncSetAttribute(staged_fused_kernel<DT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStagedSmemBudget) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, staged_fused_kernel<DT>, kThreads,
+                                                          kStagedSmemBudget) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        return occ;
+    }();
+    if (resident < 1)
+        return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
+    const int64_t want = (int64_t)sms * resident;
+    const unsigned grid = (unsigned)(tiles < want ? tiles : want);
+    staged_fused_kernel<DT><<<grid, kThreads, p.stages * staged_stage_bytes(p.world), stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+int launch_staged(const PassArgs &a, cudaStream_t stream)
+{
+    const zero_layout &L = *a.lay;
+    const int stages = staged_stages(L.world);
+    if (a.rank >= 0 || a.host_state || half_reduce(a.dtype) || L.world > kStagedMaxWorld ||
+        stages < 2 || L.padded_numel <= 0)
+        return 1;
+    StagedParams p{};
+    for (int q = 0; q < L.world; ++q)
+        p.g[q] = static_cast<const uint16_t *>(a.grads[q]);
+    p.world = L.world;
+    p.stages = stages;
+    p.n = L.padded_numel;
+    const zero_adam_cfg &c = *a.cfg;
+    p.cfg = CfgDev{c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, c.max_grad_norm,
+                   c.adamw ? 1 : 0, c.bias_correction ? 1 : 0};
+    p.state = a.state;
+    p.w0 = p.wo0 = a.master[0];
+    p.w1 = p.wo1 = a.master[1];
+    p.m0 = p.mo0 = a.m[0];
+    p.m1 = p.mo1 = a.m[1];
+    p.v0 = p.vo0 = a.v[0];
+    p.v1 = p.vo1 = a.v[1];
+    p.par0 = static_cast<uint16_t *>(a.params[0]);
+    p.par1 = static_cast<uint16_t *>(a.params[1]);
+    return is_bf16(a.dtype) ? launch_staged_dt<ZERO_BF16>(p, stream)
+                            : launch_staged_dt<ZERO_F16>(p, stream);
+}
+
 // One step (one or two passes, then the finalize) in the given modes.
 int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream)
 {
     int rc, gx = 1;
     if (a.lay->padded_numel > 0) {
         if (!clip) {
-            if ((rc = run(a, one_pass, stream, &gx)))
+            rc = one_pass == M_FUSED ? launch_staged(a, stream) : 1;
+            if (rc == 1)
+                rc = run(a, one_pass, stream, &gx);
+            if (rc)
                 return rc;
         } else {
             if ((rc = run(a, pass1, stream, &gx)))
