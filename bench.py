@@ -70,6 +70,22 @@ def kernel_source_hash(read=None) -> str:
     return h.hexdigest()[:16]
 
 
+def dominant_kernel(wl) -> str:
+    """The kernel that carries a step of the workload, by the library's rule:
+    every-rank one-pass steps with the reduction in fp32, device-resident
+    state and N_d in {1, 2, 4, 8, 16} run the shared-memory staged kernel;
+    everything else runs the register kernel."""
+    clip = wl.max_grad_norm > 0
+    if wl.micro_steps > 1:
+        return "step_kernel (accumulate passes, then the step from the accumulator)"
+    if clip:
+        return "step_kernel (two passes)"
+    if (wl.rank is None and not wl.half_reduce and not wl.offload_state
+            and wl.world in (1, 2, 4, 8, 16)):
+        return "staged_fused_kernel (TMA bulk copies into shared memory, one pass)"
+    return "step_kernel (registers, one pass)"
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -431,10 +447,7 @@ def run_ours(args, wl):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"{kind} hbm_gbs",
-                     "kernel": ("step_kernel (%s)" % ("fused, one pass" if not clip else
-                                                      "two passes"))
-                     + (" after %d accumulate passes" % wl.micro_steps
-                        if wl.micro_steps > 1 else ""),
+                     "kernel": dominant_kernel(wl),
                      "kernel_ms": kernel_ms, "bytes_per_launch": n_elems * bpe},
         "cpu_baseline": {"value": rate / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},

@@ -431,10 +431,10 @@ def test_mixed_residence_is_rejected():
 def test_staged_path_matches_register_path(world, dtype):
     """An every-rank one-pass step (the shared-memory staged kernel for
     N_d <= 16) equals, bit for bit, the same step run rank by rank (the
-    register kernel of one-rank views), over a ragged vector and a skipped
-    step."""
+    register kernel of one-rank views), over a ragged vector.  (No overflow
+    is injected: a one-rank view tests only its own partition for NaN/Inf.)"""
     wl = CFG1.replace(numels=(777_777, 4097, 3), world=world, dtype=dtype, steps=3,
-                      inject_at=((2, world - 1, 5000),), dynamic_scale=True)
+                      inject_at=())
     full = Lockstep(wl)
     parts = [Lockstep(wl.replace(rank=r)) for r in range(world)]
     for s in range(1, wl.steps + 1):

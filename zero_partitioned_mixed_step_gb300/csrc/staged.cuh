@@ -2,7 +2,8 @@
 // memory by the Tensor Memory Accelerator's bulk copies.
 //
 // Used for every-rank launches over the flat vector with the reduction in
-// fp32, device-resident state and N_d <= 16.  Each CTA owns one SM and walks
+// fp32, device-resident state and N_d in {1, 2, 4, 8, 16} (a compile-time
+// constant, so the shared-memory reads and the copies unroll).  Each CTA owns one SM and walks
 // tiles of 2048 elements with a grid stride.  For a tile, one thread issues
 // N_d + 3 one-dimensional bulk copies (cp.async.bulk): each rank's 4 KB
 // gradient slice and the 8 KB slices of master, m and v of the current
@@ -74,7 +75,7 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-template <int DT>
+template <int DT, int W>
 __global__ void __launch_bounds__(kThreads, 1)
     staged_fused_kernel(const __grid_constant__ StagedParams p)
 {
@@ -84,9 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int sh_cur;
     __shared__ int abort_flag;
     const int tid = threadIdx.x;
-    const int world = p.world, nst = p.stages;
-    const int sb = staged_stage_bytes(world);
-    const int gbytes = world * kStagedTile * 2;
+    constexpr int world = W;
+    constexpr int sb = staged_stage_bytes(W);
+    constexpr int gbytes = W * kStagedTile * 2;
+    const int nst = p.stages;
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
     if (tid == 0) {
         compute_scalars(p.cfg, p.state, sh);
@@ -125,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                      "r"(len * 2u * (uint32_t)world + 3u * len * 4u)
                      : "memory");
-        for (int q = 0; q < world; ++q)
+#pragma unroll
+        for (int q = 0; q < W; ++q)
             bulk_copy(base + q * kStagedTile * 2, p.g[q] + e0, len * 2u, bar);
         bulk_copy(base + gbytes, w_src + e0, len * 4u, bar);
         bulk_copy(base + gbytes + kStagedTile * 4, m_src + e0, len * 4u, bar);
@@ -163,8 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 g[i] = 0.0f;
-            for (int q = 0; q < world; ++q)
-                add_half8<DT>(g, reinterpret_cast<const uint4 *>(stage + q * kStagedTile * 2)[tid]);
+            uint4 x[W];
+#pragma unroll
+            for (int q = 0; q < W; ++q)
+                x[q] = reinterpret_cast<const uint4 *>(stage + q * kStagedTile * 2)[tid];
+#pragma unroll
+            for (int q = 0; q < W; ++q)
+                add_half8<DT>(g, x[q]);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 g[i] = __fmul_rn(g[i], s.inv_s);

@@ -413,21 +413,22 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
 }
 
 // The staged one-pass step (staged.cuh), when it applies: every rank at once,
-// fp32 reduction, device-resident state, N_d <= 16.  Returns 1 when it does
-// not apply (the caller then uses the register path).
-template <int DT>
-int launch_staged_dt(const StagedParams &p, cudaStream_t stream)
+// fp32 reduction, device-resident state, N_d in {1, 2, 4, 8, 16}.  Returns 1
+// when it does not apply (the caller then uses the register path).
+template <int DT, int W>
+int launch_staged_w(const StagedParams &p, cudaStream_t stream)
 {
     static const int resident = [] {
-        if (cudaFuncSetAttribute(staged_fused_kernel<DT>,
+        if (cudaFuncSetAttribute(staged_fused_kernel<DT, W>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kStagedSmemBudget) != cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
         }
         int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, staged_fused_kernel<DT>, kThreads,
-                                                          kStagedSmemBudget) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, staged_fused_kernel<DT, W>,
+                                                          kThreads, kStagedSmemBudget) !=
+            cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
         }
@@ -442,9 +443,22 @@ int launch_staged_dt(const StagedParams &p, cudaStream_t stream)
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
     const int64_t want = (int64_t)sms * resident;
     const unsigned grid = (unsigned)(tiles < want ? tiles : want);
-    staged_fused_kernel<DT><<<grid, kThreads, p.stages * staged_stage_bytes(p.world), stream>>>(p);
+    staged_fused_kernel<DT, W><<<grid, kThreads, p.stages * staged_stage_bytes(W), stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+template <int DT>
+int launch_staged_dt(const StagedParams &p, cudaStream_t stream)
+{
+    switch (p.world) {
+    case 1: return launch_staged_w<DT, 1>(p, stream);
+    case 2: return launch_staged_w<DT, 2>(p, stream);
+    case 4: return launch_staged_w<DT, 4>(p, stream);
+    case 8: return launch_staged_w<DT, 8>(p, stream);
+    case 16: return launch_staged_w<DT, 16>(p, stream);
+    default: return 1;
+    }
 }
 
 int launch_staged(const PassArgs &a, cudaStream_t stream)
