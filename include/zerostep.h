@@ -71,6 +71,14 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__) || defined(__clang__)
+/* The library is built with hidden visibility: only the entry points below
+ * are exported, so two copies loaded in one process keep their own state. */
+#define ZERO_API __attribute__((visibility("default")))
+#else
+#define ZERO_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -166,10 +174,10 @@ typedef struct {
 } zero_step_state;
 
 /* Human-readable text for a return code (static storage). */
-const char *zero_strerror(int code);
+ZERO_API const char *zero_strerror(int code);
 
 /* ABI version: 1. */
-int zero_version(void);
+ZERO_API int zero_version(void);
 
 /*
  * Step (a1): the partition layout.  Host-only, pure.
@@ -184,16 +192,17 @@ int zero_version(void);
  * rank; the floor division there is read as padding so no element is lost);
  * "DeepSpeed ZeRO", "Constant Size Buffer" (buckets).
  */
-int zero_partition_layout(int n_tensors, const int64_t *numel, int world, int align_elems,
-                          int64_t bucket_numel, int64_t *tensor_offset_out, zero_layout *out);
+ZERO_API int zero_partition_layout(int n_tensors, const int64_t *numel, int world,
+                                   int align_elems, int64_t bucket_numel,
+                                   int64_t *tensor_offset_out, zero_layout *out);
 
 /* Fill *host_state with the state before the first step: t = 0, beta powers
  * 1, loss_scale (a positive power of two), clip_coef 1, everything else 0. */
-int zero_state_init(zero_step_state *host_state, float loss_scale);
+ZERO_API int zero_state_init(zero_step_state *host_state, float loss_scale);
 
 /* Bytes of workspace the device-side reductions need for a group of `world`
  * ranks (a few tens of KB).  Its contents need no initialisation. */
-size_t zero_workspace_bytes(int world);
+ZERO_API size_t zero_workspace_bytes(int world);
 
 /*
  * Step (a2): reduce-scatter sum, g[j] = sum over q = 0 .. world-1 of
@@ -205,9 +214,9 @@ size_t zero_workspace_bytes(int world);
  *    order.  rank = r: r's partition; g_out (owned_numel floats) in r's order.
  * Pages: "zero-optimizer", 2.5 ReduceScatter; "DeepSpeed ZeRO", ZeRO Stage 2.
  */
-int zero_reduce_scatter_sum(const void *const *grads, int grads_are_slices, zero_dtype dtype,
-                            const zero_layout *layout, int rank, float *g_out,
-                            zero_stream_t stream);
+ZERO_API int zero_reduce_scatter_sum(const void *const *grads, int grads_are_slices,
+                                     zero_dtype dtype, const zero_layout *layout, int rank,
+                                     float *g_out, zero_stream_t stream);
 
 /*
  * Step (a4): *flag_dev |= 1 if any g[j] * inv_scale (j < n) is NaN or +-Inf;
@@ -216,8 +225,8 @@ int zero_reduce_scatter_sum(const void *const *grads, int grads_are_slices, zero
  * aligned.
  * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "权重更新的触发条件".
  */
-int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *flag_dev,
-                        zero_stream_t stream);
+ZERO_API int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *flag_dev,
+                                 zero_stream_t stream);
 
 /*
  * Step (a5): *sumsq_dev = sum over j < n of (g[j] * inv_scale)^2, accumulated
@@ -228,8 +237,8 @@ int zero_check_overflow(const float *g, int64_t n, float inv_scale, int32_t *fla
  * Pages: "zero-optimizer", "一. 优化前" (gradient-norm computation over fused
  * buffers); the clip rule itself is a reading (see zero_adam_cfg).
  */
-int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
-                   size_t ws_bytes, zero_stream_t stream);
+ZERO_API int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
+                            size_t ws_bytes, zero_stream_t stream);
 
 /*
  * Gradient accumulation, one micro-step: the reduce-scatter sum of the N_d
@@ -244,9 +253,9 @@ int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev
  * after every backward and accumulates its 1/N_d slice) and the page's memory
  * section (the optional fp32 gradient copy for accumulating in fp32).
  */
-int zero_reduce_scatter_accumulate(const void *const *grads, int grads_are_slices,
-                                   zero_dtype dtype, const zero_layout *layout, int rank,
-                                   float *acc, int add, zero_stream_t stream);
+ZERO_API int zero_reduce_scatter_accumulate(const void *const *grads, int grads_are_slices,
+                                            zero_dtype dtype, const zero_layout *layout, int rank,
+                                            float *acc, int add, zero_stream_t stream);
 
 /*
  * The whole step (a3)-(a8) with the gradient taken from an fp32 accumulator
@@ -259,11 +268,12 @@ int zero_reduce_scatter_accumulate(const void *const *grads, int grads_are_slice
  * two passes over acc, slots may alias, with clipping).
  * Pages: as zero_step_fused and zero_reduce_scatter_accumulate.
  */
-int zero_step_fused_accumulated(const float *acc, zero_dtype dtype, const zero_layout *layout,
-                                int rank, float *const master[2], float *const m[2],
-                                float *const v[2], void *const params[2],
-                                const zero_adam_cfg *cfg, zero_step_state *state_dev, void *ws,
-                                size_t ws_bytes, zero_stream_t stream);
+ZERO_API int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
+                                         const zero_layout *layout, int rank,
+                                         float *const master[2], float *const m[2],
+                                         float *const v[2], void *const params[2],
+                                         const zero_adam_cfg *cfg, zero_step_state *state_dev,
+                                         void *ws, size_t ws_bytes, zero_stream_t stream);
 
 /*
  * zero_grad_norm for callers that cannot allocate device memory.  The pages
@@ -291,8 +301,8 @@ int zero_step_fused_accumulated(const float *acc, zero_dtype dtype, const zero_l
  *  that first call before any stream capture.
  */
 #define ZERO_NOALLOC_PARTIALS 4096
-int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *sumsq_dev,
-                           zero_stream_t stream);
+ZERO_API int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *sumsq_dev,
+                                    zero_stream_t stream);
 
 /*
  * Steps (a3), (a5 clip), (a6), (a7) on n elements in place, for the reduced
@@ -305,9 +315,9 @@ int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *s
  * afterwards to commit the step.
  * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "以 AdaW 为例" and "权重更新的触发条件".
  */
-int zero_adam_step(const float *g, float *master, float *m, float *v, void *half_out,
-                   zero_dtype dtype, int64_t n, const zero_adam_cfg *cfg,
-                   const zero_step_state *state_dev, zero_stream_t stream);
+ZERO_API int zero_adam_step(const float *g, float *master, float *m, float *v, void *half_out,
+                            zero_dtype dtype, int64_t n, const zero_adam_cfg *cfg,
+                            const zero_step_state *state_dev, zero_stream_t stream);
 
 /*
  * Step (a8): end a step.  If state_dev->found_inf: overflow = 1, skipped += 1,
@@ -317,8 +327,8 @@ int zero_adam_step(const float *g, float *master, float *m, float *v, void *half
  * ping-pong slot cur is toggled.  found_inf is cleared either way.
  * Pages: "DeepSpeed ZeRO", ZeRO Stage 1, "权重更新的触发条件"; "配置说明".
  */
-int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int flip_slot,
-                       zero_stream_t stream);
+ZERO_API int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int flip_slot,
+                                zero_stream_t stream);
 
 /*
  * The whole step (a2)-(a8), fused.
@@ -351,11 +361,12 @@ int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int
  * Pages: all of the above; the ping-pong slots are this library's way to
  * skip a step bit-exactly without a second pass over the gradients.
  */
-int zero_step_fused(const void *const *grads, int grads_are_slices, zero_dtype dtype,
-                    const zero_layout *layout, int rank, float *const master[2],
-                    float *const m[2], float *const v[2], void *const params[2], float *g_stage,
-                    const zero_adam_cfg *cfg, zero_step_state *state_dev, void *ws,
-                    size_t ws_bytes, zero_stream_t stream);
+ZERO_API int zero_step_fused(const void *const *grads, int grads_are_slices, zero_dtype dtype,
+                             const zero_layout *layout, int rank, float *const master[2],
+                             float *const m[2], float *const v[2], void *const params[2],
+                             float *g_stage, const zero_adam_cfg *cfg,
+                             zero_step_state *state_dev, void *ws, size_t ws_bytes,
+                             zero_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -42,6 +42,21 @@ def test_exports_every_declared_symbol(zs):
     assert set(names) == set(zs._abi.SIGNATURES)
 
 
+def test_exports_nothing_else(zs):
+    """Only the declared entry points are dynamic symbols of the library
+    (it is built with hidden visibility), so internal state such as cached
+    launch attributes stays private to each loaded copy."""
+    import shutil
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not installed")
+    out = subprocess.run([nm, "-D", "--defined-only", zs._build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    exported -= {"_init", "_fini"}
+    assert exported == set(declared_functions())
+
+
 def test_structs_match_header(tmp_path, zs):
     src = tmp_path / "off.c"
     fields = {"zero_layout": zs.Layout, "zero_adam_cfg": zs.AdamCfg,

@@ -29,7 +29,7 @@ def nvcc() -> str:
         raise RuntimeError("nvcc not found (install the CUDA toolkit or set CUDA_HOME)")
     return path
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-Wall", "-I", INCLUDE, *ARCH]
+              "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-Wall", "-I", INCLUDE, *ARCH]
 
 
 def _sources():

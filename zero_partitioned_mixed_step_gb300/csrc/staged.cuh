@@ -3,13 +3,14 @@
 //
 // Used for every-rank launches over the flat vector with the reduction in
 // fp32, device-resident state and N_d in {1, 2, 4, 8, 16} (a compile-time
-// constant, so the shared-memory reads and the copies unroll).  Each CTA owns one SM and walks
-// tiles of 2048 elements with a grid stride.  For a tile, one thread issues
-// N_d + 3 one-dimensional bulk copies (cp.async.bulk): each rank's 4 KB
-// gradient slice and the 8 KB slices of master, m and v of the current
-// ping-pong slot, all completing on the stage's mbarrier.  The next tiles'
-// copies are in flight while the 256 threads reduce, update and store the
-// current one (2 to 4 stages, by N_d).  Results leave with 256-bit stores
+// constant, so the shared-memory reads and the copies unroll).  Each CTA walks
+// tiles of kStagedThreads x 8 elements with a grid stride.  For a tile, one
+// thread issues N_d + 3 one-dimensional bulk copies (cp.async.bulk, marked
+// evict-first in L2): each rank's gradient slice and the slices of master, m
+// and v of the current ping-pong slot, all completing on the stage's
+// mbarrier.  The next tiles' copies are in flight while the threads reduce,
+// update and store the current one (as many stages as the shared-memory
+// budget holds, 2 to kStagedMaxStages).  Results leave with 256-bit stores
 // (state) and 16-byte stores (parameters) to the other slot.  The arithmetic
 // is exactly the register path's, so the two give the same bits.
 //
@@ -24,8 +25,9 @@
 
 namespace zs {
 
-constexpr int kStagedTile = kThreads * kUnit;    // 2048 elements per tile
-constexpr int kStagedMaxStages = 4;
+constexpr int kStagedThreads = 256;
+constexpr int kStagedTile = kStagedThreads * kUnit;  // elements per tile
+constexpr int kStagedMaxStages = 8;
 constexpr int kStagedMaxWorld = 16;
 constexpr int kStagedSmemBudget = 200 * 1024;     // dynamic shared memory per CTA
 constexpr long long kStageSpinLimit = 1ll << 26;  // polls of try_wait (seconds)
@@ -66,17 +68,18 @@ __device__ __forceinline__ bool stage_ready(uint32_t bar, uint32_t parity)
 }
 
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar)
+                                          uint32_t bar, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
         :
-        : "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
 template <int DT, int W>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kStagedThreads, 1)
     staged_fused_kernel(const __grid_constant__ StagedParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *m_dst = cur ? p.mo0 : p.mo1;
     float *v_dst = cur ? p.vo0 : p.vo1;
     uint16_t *out = cur ? p.par0 : p.par1;
+    const uint64_t pol = evict_first_policy();
 
     // Tile k of this CTA into stage k % nst (thread 0 only).
     auto issue = [&](int64_t k) {
@@ -129,16 +133,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
 #pragma unroll
         for (int q = 0; q < W; ++q)
-            bulk_copy(base + q * kStagedTile * 2, p.g[q] + e0, len * 2u, bar);
-        bulk_copy(base + gbytes, w_src + e0, len * 4u, bar);
-        bulk_copy(base + gbytes + kStagedTile * 4, m_src + e0, len * 4u, bar);
-        bulk_copy(base + gbytes + 2 * kStagedTile * 4, v_src + e0, len * 4u, bar);
+            bulk_copy(base + q * kStagedTile * 2, p.g[q] + e0, len * 2u, bar, pol);
+        bulk_copy(base + gbytes, w_src + e0, len * 4u, bar, pol);
+        bulk_copy(base + gbytes + kStagedTile * 4, m_src + e0, len * 4u, bar, pol);
+        bulk_copy(base + gbytes + 2 * kStagedTile * 4, v_src + e0, len * 4u, bar, pol);
     };
 
     if (tid == 0)
         for (int k = 0; k < nst; ++k)
             issue(k);
-    const uint64_t pol = evict_first_policy();
     bool bad = false;
     int64_t k = 0;
     for (;; ++k) {

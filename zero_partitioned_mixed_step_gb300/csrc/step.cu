@@ -427,7 +427,7 @@ int launch_staged_w(const StagedParams &p, cudaStream_t stream)
         }
         int occ = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, staged_fused_kernel<DT, W>,
-                                                          kThreads, kStagedSmemBudget) !=
+                                                          kStagedThreads, kStagedSmemBudget) !=
             cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
@@ -443,7 +443,8 @@ int launch_staged_w(const StagedParams &p, cudaStream_t stream)
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
     const int64_t want = (int64_t)sms * resident;
     const unsigned grid = (unsigned)(tiles < want ? tiles : want);
-    staged_fused_kernel<DT, W><<<grid, kThreads, p.stages * staged_stage_bytes(W), stream>>>(p);
+    staged_fused_kernel<DT, W>
+        <<<grid, kStagedThreads, p.stages * staged_stage_bytes(W), stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
