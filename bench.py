@@ -73,15 +73,15 @@ def kernel_source_hash(read=None) -> str:
 def dominant_kernel(wl) -> str:
     """The kernel that carries a step of the workload, by the library's rule:
     every-rank one-pass steps with the reduction in fp32, device-resident
-    state and N_d in {1, 2, 4, 8, 16} run the shared-memory staged kernel;
-    everything else runs the register kernel."""
+    state and N_d = 16 run the shared-memory staged kernel; everything else
+    runs the register kernel."""
     clip = wl.max_grad_norm > 0
     if wl.micro_steps > 1:
         return "step_kernel (accumulate passes, then the step from the accumulator)"
     if clip:
         return "step_kernel (two passes)"
     if (wl.rank is None and not wl.half_reduce and not wl.offload_state
-            and wl.world in (1, 2, 4, 8, 16)):
+            and wl.world == 16):
         return "staged_fused_kernel (TMA bulk copies into shared memory, one pass)"
     return "step_kernel (registers, one pass)"
 
@@ -465,12 +465,14 @@ def run_ours(args, wl):
 
 
 def run_e2e(z, grads, wl, args, steps: int = 5):
-    """Host -> device copies of every rank's gradient from pinned memory, the
-    step, and the device -> host read of the step state, all timed."""
+    """Host -> device copies of every rank's gradient from page-locked host
+    memory (the library's zero_host_alloc blocks), the step, and the device ->
+    host read of the step state, all timed."""
     import torch
+    import zero_partitioned_mixed_step_gb300 as zs
     try:
-        host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in grads]
-    except RuntimeError as e:  # not enough pinnable host memory
+        host = [zs.host_empty(g.numel(), g.dtype) for g in grads]
+    except (RuntimeError, zs.ZeroError) as e:  # not enough pinnable host memory
         return {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                 "unavailable": f"pinned host buffers: {str(e).splitlines()[0]}"}
     for h, g in zip(host, grads):

@@ -205,6 +205,28 @@ ZERO_API int zero_state_init(zero_step_state *host_state, float loss_scale);
 ZERO_API size_t zero_workspace_bytes(int world);
 
 /*
+ * Page-locked host memory for the buffers a step exchanges with the host:
+ * gradients that the caller copies in before a step, or the fp32 master
+ * weights and moments kept in CPU memory as in ZeRO-Offload ("千亿参数模型如何
+ * 塞进有限显卡…", "ZeRO-Offload：利用CPU内存").  The memory is mapped into the
+ * device's address space, so a kernel may also read or write it directly
+ * (zero_step_fused does so for offloaded state).  On a GB300 host these
+ * blocks move over NVLink-C2C at the link's full rate; pinned blocks from
+ * general-purpose caching allocators were measured at half that rate.
+ *  zero_host_alloc: *out = a new block of `bytes` bytes (at least 256-byte
+ *    aligned, contents undefined); bytes = 0 gives *out = NULL and ZERO_OK.
+ *    ZERO_EINVAL if out is NULL; a failed allocation returns
+ *    ZERO_ECUDA_BASE - cudaError_t with *out = NULL.
+ *  zero_host_free: releases a block from zero_host_alloc (NULL is a no-op).
+ *    It synchronises with the device like cudaFreeHost: no copy or kernel
+ *    may still use the block.  The caller owns each block until it frees it.
+ * The pages have no counterpart for this call; it is the runtime's memory
+ * management for the host side of the step.
+ */
+ZERO_API int zero_host_alloc(size_t bytes, void **out);
+ZERO_API int zero_host_free(void *p);
+
+/*
  * Step (a2): reduce-scatter sum, g[j] = sum over q = 0 .. world-1 of
  * float(grads[q][.]) in ascending q, fp32, not unscaled.
  *  grads: HOST array of `world` DEVICE pointers, one gradient buffer per rank.

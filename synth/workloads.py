@@ -153,4 +153,11 @@ HALFRED_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-halfreduce", half_reduce=T
 OFFLOAD_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-offload", offload_state=True, steps=10,
                             inject_every=0)
 
-BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, ACCUM_CFG3, HALFRED_CFG3, OFFLOAD_CFG3)}
+# A smaller case of the 7.5B rank-0 shard for detailed profiles: a 600M flat
+# vector over the same 64 ranks gives rank 0 9.375M elements (one launch
+# streams 1.44 GB, far above L2; ~4 GB on the device, most of it the two
+# slots of the full half-precision parameter vector).
+PROFILE_CFG4 = CFG4.replace(name="600M-shard-nd64-rank0-fp16", numels=(600_000_000,))
+
+BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, PROFILE_CFG4, ACCUM_CFG3, HALFRED_CFG3,
+                                     OFFLOAD_CFG3)}

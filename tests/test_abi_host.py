@@ -35,7 +35,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(zs):
     names = declared_functions()
-    assert len(names) == 14, names
+    assert len(names) == 16, names
     so = ctypes.CDLL(zs._build.LIB)
     for n in names:
         assert hasattr(so, n), n
@@ -55,6 +55,18 @@ def test_exports_nothing_else(zs):
     exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
     exported -= {"_init", "_fini"}
     assert exported == set(declared_functions())
+
+
+def test_host_alloc_arguments(zs):
+    """zero_host_alloc / zero_host_free argument handling that needs no
+    device: a zero-byte block is NULL, a NULL result pointer is rejected,
+    freeing NULL is a no-op."""
+    L = zs._abi.lib()
+    p = ctypes.c_void_p(1234)
+    assert L.zero_host_alloc(0, ctypes.byref(p)) == 0 and p.value is None
+    assert L.zero_host_alloc(64, None) == -1
+    assert L.zero_host_free(None) == 0
+    assert zs.host_empty(0, zs.torch_dtype(zs.F16)).numel() == 0
 
 
 def test_structs_match_header(tmp_path, zs):

@@ -28,7 +28,7 @@ __all__ = [
     "adam_cfg", "new_state", "read_state", "state_field_ptr", "zero_partition_layout",
     "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
     "zero_grad_norm", "zero_grad_norm_noalloc", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
-    "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated",
+    "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated", "host_empty",
 ]
 
 _TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
@@ -100,6 +100,34 @@ def zero_workspace_bytes(world: int) -> int:
     if n == 0:
         raise ZeroError("zero_workspace_bytes", -1)
     return n
+
+
+class _HostBlock:
+    """One zero_host_alloc block, released when the last tensor over it is
+    gone (the tensor keeps the buffer object alive, which keeps the block)."""
+
+    def __init__(self, nbytes: int):
+        p = ctypes.c_void_p()
+        check("zero_host_alloc", lib().zero_host_alloc(nbytes, ctypes.byref(p)))
+        self.ptr = p.value
+
+    def __del__(self):
+        if self.ptr:
+            lib().zero_host_free(self.ptr)
+            self.ptr = None
+
+
+def host_empty(numel: int, dtype: torch.dtype) -> torch.Tensor:
+    """A CPU tensor of `numel` elements in page-locked host memory from
+    zero_host_alloc (contents undefined).  Copies from and to it run at the
+    host link's full rate, and kernels may read or write it directly."""
+    nbytes = int(numel) * torch.empty(0, dtype=dtype).element_size()
+    if nbytes == 0:
+        return torch.empty(0, dtype=dtype)
+    block = _HostBlock(nbytes)
+    buf = (ctypes.c_uint8 * nbytes).from_address(block.ptr)
+    buf._block = block
+    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype)
 
 
 def adam_cfg(lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
@@ -233,8 +261,9 @@ class ZeroStep:
     double-buffered so an overflow step can be skipped in one pass; with
     clipping they are updated in place and the reduced gradient is staged in
     fp32 between the two passes when that reads fewer bytes (N_d > 4).
-    offload_state keeps master, m and v in pinned host memory (ZeRO-Offload
-    style; the GPU reaches them over the host link).
+    offload_state keeps master, m and v in page-locked host memory from
+    zero_host_alloc (ZeRO-Offload style; the GPU reaches them over the host
+    link).
     """
 
     def __init__(self, numels: Sequence[int], world: int, dtype: int, cfg: AdamCfg,
@@ -253,11 +282,16 @@ class ZeroStep:
         if offload_state and clip:
             raise ValueError("offloaded optimizer state supports the one-pass step (no clip)")
         f32 = dict(dtype=torch.float32, device=device)
-        st32 = dict(dtype=torch.float32, pin_memory=True) if offload_state else f32
         slots = 1 if clip else 2
-        self.master = [torch.zeros(self.n_state, **st32) for _ in range(slots)]
-        self.m = [torch.zeros(self.n_state, **st32) for _ in range(slots)]
-        self.v = [torch.zeros(self.n_state, **st32) for _ in range(slots)]
+
+        def state_buffer():
+            if offload_state:
+                return host_empty(self.n_state, torch.float32).zero_()
+            return torch.zeros(self.n_state, **f32)
+
+        self.master = [state_buffer() for _ in range(slots)]
+        self.m = [state_buffer() for _ in range(slots)]
+        self.v = [state_buffer() for _ in range(slots)]
         self.params = [torch.zeros(L.padded_numel, dtype=hdt, device=device) for _ in range(slots)]
         if slots == 1:
             for lst in (self.master, self.m, self.v, self.params):
@@ -313,7 +347,7 @@ class ZeroStep:
         host buffers stand for each) and accumulated before the step."""
         s = stream if stream is not None else torch.cuda.current_stream()
         if getattr(self, "_state_host", None) is None:
-            self._state_host = torch.empty(64, dtype=torch.uint8, pin_memory=True)
+            self._state_host = host_empty(64, torch.uint8)
         with torch.cuda.stream(s):
             for k in range(micro_steps):
                 for h, d in zip(host_grads, device_grads):

@@ -58,6 +58,8 @@ SIGNATURES = {
                                ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(Layout)], _I),
     "zero_state_init": ([ctypes.POINTER(StepState), ctypes.c_float], _I),
     "zero_workspace_bytes": ([_I], ctypes.c_size_t),
+    "zero_host_alloc": ([ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)], _I),
+    "zero_host_free": ([_P], _I),
     "zero_reduce_scatter_sum": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _P, _P], _I),
     "zero_check_overflow": ([_P, _I64, ctypes.c_float, _P, _P], _I),
     "zero_grad_norm": ([_P, _I64, ctypes.c_float, _P, _P, ctypes.c_size_t, _P], _I),

@@ -1,7 +1,9 @@
 // Host-only entry points: the partition layout (step a1), the initial step
-// state, the workspace size and the error strings.
+// state, the workspace size, page-locked host blocks and the error strings.
 #include <cmath>
 #include <cstring>
+
+#include <cuda_runtime.h>
 
 #include "internal.h"
 
@@ -65,7 +67,7 @@ const char *zero_strerror(int code)
     case ZERO_EINVAL: return "invalid argument";
     case ZERO_EALIGN: return "buffer not aligned (32 bytes for fp32, 16 for half)";
     case ZERO_ESPACE: return "workspace too small";
-    default: return code <= ZERO_ECUDA_BASE ? "CUDA launch failed" : "unknown error";
+    default: return code <= ZERO_ECUDA_BASE ? "CUDA call failed" : "unknown error";
     }
 }
 
@@ -139,6 +141,34 @@ size_t zero_workspace_bytes(int world)
     if (world < 1 || world > ZERO_MAX_WORLD)
         return 0;
     return (size_t)zs::kWsHeader + sizeof(double) * (size_t)(zs::kMaxCtas + 2 * world);
+}
+
+int zero_host_alloc(size_t bytes, void **out)
+{
+    if (!out)
+        return ZERO_EINVAL;
+    *out = nullptr;
+    if (bytes == 0)
+        return ZERO_OK;
+    const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        *out = nullptr;
+        return zs::cuda_error(e);
+    }
+    return ZERO_OK;
+}
+
+int zero_host_free(void *p)
+{
+    if (!p)
+        return ZERO_OK;
+    const cudaError_t e = cudaFreeHost(p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return zs::cuda_error(e);
+    }
+    return ZERO_OK;
 }
 
 }  // extern "C"

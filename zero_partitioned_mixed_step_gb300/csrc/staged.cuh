@@ -2,15 +2,18 @@
 // memory by the Tensor Memory Accelerator's bulk copies.
 //
 // Used for every-rank launches over the flat vector with the reduction in
-// fp32, device-resident state and N_d in {1, 2, 4, 8, 16} (a compile-time
-// constant, so the shared-memory reads and the copies unroll).  Each CTA walks
-// tiles of kStagedThreads x 8 elements with a grid stride.  For a tile, one
-// thread issues N_d + 3 one-dimensional bulk copies (cp.async.bulk, marked
-// evict-first in L2): each rank's gradient slice and the slices of master, m
-// and v of the current ping-pong slot, all completing on the stage's
-// mbarrier.  The next tiles' copies are in flight while the threads reduce,
-// update and store the current one (as many stages as the shared-memory
-// budget holds, 2 to kStagedMaxStages).  Results leave with 256-bit stores
+// fp32, device-resident state and N_d = 16 (a compile-time constant, so the
+// shared-memory reads and the copies unroll).  Measured on GB300 against the
+// register kernel on the same buffers, it is 0.7 % faster at N_d = 16 and
+// slower at N_d = 8 (1 %) and N_d = 4 (8 %), where the fp32 state dominates
+// the traffic; with 256 threads and one CTA per SM it lost at every N_d.
+// Each CTA (128 threads, two per SM) walks tiles of 1024 elements with a grid
+// stride.  For a tile, one thread issues N_d + 3 one-dimensional bulk copies
+// (cp.async.bulk, marked evict-first in L2): each rank's 2 KB gradient slice
+// and the 4 KB slices of master, m and v of the current ping-pong slot, all
+// completing on the stage's mbarrier.  The next tile's copies are in flight
+// while the threads reduce, update and store the current one (two 44 KB
+// stages per CTA).  Results leave with 256-bit stores
 // (state) and 16-byte stores (parameters) to the other slot.  The arithmetic
 // is exactly the register path's, so the two give the same bits.
 //
@@ -25,11 +28,11 @@
 
 namespace zs {
 
-constexpr int kStagedThreads = 256;
+constexpr int kStagedThreads = 128;
 constexpr int kStagedTile = kStagedThreads * kUnit;  // elements per tile
 constexpr int kStagedMaxStages = 8;
-constexpr int kStagedMaxWorld = 16;
-constexpr int kStagedSmemBudget = 200 * 1024;     // dynamic shared memory per CTA
+constexpr int kStagedWorld = 16;                  // the one N_d it serves
+constexpr int kStagedSmemBudget = 100 * 1024;     // dynamic shared memory per CTA
 constexpr long long kStageSpinLimit = 1ll << 26;  // polls of try_wait (seconds)
 
 // Bytes of one stage for a group of `world` ranks.
@@ -45,8 +48,7 @@ inline int staged_stages(int world)
 }
 
 struct StagedParams {
-    const uint16_t *g[kStagedMaxWorld];
-    int32_t world;
+    const uint16_t *g[kStagedWorld];
     int32_t stages;
     int64_t n;  // padded flat elements (a multiple of 64)
     CfgDev cfg;

@@ -413,8 +413,8 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
 }
 
 // The staged one-pass step (staged.cuh), when it applies: every rank at once,
-// fp32 reduction, device-resident state, N_d in {1, 2, 4, 8, 16}.  Returns 1
-// when it does not apply (the caller then uses the register path).
+// fp32 reduction, device-resident state, N_d = 16.  Returns 1 when it does not
+// apply (the caller then uses the register path).
 template <int DT, int W>
 int launch_staged_w(const StagedParams &p, cudaStream_t stream)
 {
@@ -449,30 +449,16 @@ int launch_staged_w(const StagedParams &p, cudaStream_t stream)
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
 
-template <int DT>
-int launch_staged_dt(const StagedParams &p, cudaStream_t stream)
-{
-    switch (p.world) {
-    case 1: return launch_staged_w<DT, 1>(p, stream);
-    case 2: return launch_staged_w<DT, 2>(p, stream);
-    case 4: return launch_staged_w<DT, 4>(p, stream);
-    case 8: return launch_staged_w<DT, 8>(p, stream);
-    case 16: return launch_staged_w<DT, 16>(p, stream);
-    default: return 1;
-    }
-}
-
 int launch_staged(const PassArgs &a, cudaStream_t stream)
 {
     const zero_layout &L = *a.lay;
     const int stages = staged_stages(L.world);
-    if (a.rank >= 0 || a.host_state || half_reduce(a.dtype) || L.world > kStagedMaxWorld ||
+    if (a.rank >= 0 || a.host_state || half_reduce(a.dtype) || L.world != kStagedWorld ||
         stages < 2 || L.padded_numel <= 0)
         return 1;
     StagedParams p{};
     for (int q = 0; q < L.world; ++q)
         p.g[q] = static_cast<const uint16_t *>(a.grads[q]);
-    p.world = L.world;
     p.stages = stages;
     p.n = L.padded_numel;
     const zero_adam_cfg &c = *a.cfg;
@@ -487,8 +473,8 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
     p.v1 = p.vo1 = a.v[1];
     p.par0 = static_cast<uint16_t *>(a.params[0]);
     p.par1 = static_cast<uint16_t *>(a.params[1]);
-    return is_bf16(a.dtype) ? launch_staged_dt<ZERO_BF16>(p, stream)
-                            : launch_staged_dt<ZERO_F16>(p, stream);
+    return is_bf16(a.dtype) ? launch_staged_w<ZERO_BF16, kStagedWorld>(p, stream)
+                            : launch_staged_w<ZERO_F16, kStagedWorld>(p, stream);
 }
 
 // One step (one or two passes, then the finalize) in the given modes.
