@@ -48,11 +48,13 @@
  * (rank = -1) or one rank's partition (rank = r).
  *
  * Conventions for every entry point:
- *  - The caller allocates and owns every buffer; the library allocates no
- *    memory and keeps no state between calls other than read-only device
- *    properties (SM counts, resident CTAs per kernel), cached on first use.  Pointers named *_dev or documented as device pointers must
- *    be CUDA device pointers of the current device; all others are host
- *    pointers read during the call only.
+ *  - The caller allocates and owns every buffer.  The library allocates no
+ *    memory except the blocks zero_host_alloc hands to the caller.  Between
+ *    calls it keeps only read-only device properties (SM counts, resident CTAs
+ *    per kernel, cached on first use) and the one static array that
+ *    zero_grad_norm_noalloc documents.  Pointers named *_dev or documented as
+ *    device pointers must be CUDA device pointers of the current device; all
+ *    others are host pointers read during the call only.
  *  - Device work is enqueued on `stream` (NULL = the legacy default stream)
  *    and runs asynchronously; nothing synchronises the host.  Calls that use
  *    the same workspace or state must be ordered on one stream.
@@ -210,9 +212,9 @@ ZERO_API size_t zero_workspace_bytes(int world);
  * weights and moments kept in CPU memory as in ZeRO-Offload ("千亿参数模型如何
  * 塞进有限显卡…", "ZeRO-Offload：利用CPU内存").  The memory is mapped into the
  * device's address space, so a kernel may also read or write it directly
- * (zero_step_fused does so for offloaded state).  On a GB300 host these
- * blocks move over NVLink-C2C at the link's full rate; pinned blocks from
- * general-purpose caching allocators were measured at half that rate.
+ * (zero_step_fused does so for offloaded state).  The calls give C callers
+ * that have no framework allocator the same blocks a framework's pinned
+ * allocator would give.
  *  zero_host_alloc: *out = a new block of `bytes` bytes (at least 256-byte
  *    aligned, contents undefined); bytes = 0 gives *out = NULL and ZERO_OK.
  *    ZERO_EINVAL if out is NULL; a failed allocation returns
