@@ -78,6 +78,10 @@ def dominant_kernel(wl) -> str:
     clip = wl.max_grad_norm > 0
     if wl.micro_steps > 1:
         return "step_kernel (accumulate passes, then the step from the accumulator)"
+    if wl.per_bucket:
+        base = ("staged_fused_kernel" if wl.rank is None and not wl.half_reduce
+                and not wl.offload_state and wl.world == 16 else "step_kernel")
+        return base + " (one launch per bucket on two streams, then the commit)"
     if clip:
         return "step_kernel (two passes)"
     if (wl.rank is None and not wl.half_reduce and not wl.offload_state
@@ -374,18 +378,37 @@ def run_ours(args, wl):
         flush = torch.empty(64 << 20, dtype=torch.float32, device=device)
 
     micro = wl.micro_steps
+    side = [torch.cuda.Stream(device), torch.cuda.Stream(device)] if wl.per_bucket else None
+    first_bucket_done = []  # per step: event after the first bucket's launch
 
     def one_step():
         if micro > 1:  # gradient accumulation: the same buffers stand for every micro-step
             for k in range(micro):
                 z.accumulate(grads, k > 0, stream)
             z.step_accumulated(stream)
+        elif wl.per_bucket:  # one launch per bucket, alternating streams, then the commit
+            go = torch.cuda.Event()
+            go.record(stream)
+            for st in side:
+                st.wait_event(go)
+            for b in range(L.num_buckets):
+                z.step_buckets(grads, b, 1, side[b % 2])
+                if b == 0:
+                    e = torch.cuda.Event(enable_timing=True)
+                    e.record(side[0])
+                    first_bucket_done.append(e)
+            for st in side:
+                e = torch.cuda.Event()
+                e.record(st)
+                stream.wait_event(e)
+            z.commit(stream)
         else:
             z.step(grads, stream)
 
     for s in range(1, args.warmup + 1):
         one_step()
     torch.cuda.synchronize()
+    first_bucket_done.clear()
 
     nsteps = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -430,6 +453,14 @@ def run_ours(args, wl):
     traffic = recorded_traffic(wl.name)
     rate, threads, desc = oracle_sample_rate(wl)
     launches_per_step = (4 if clip else 2) + (wl.micro_steps if wl.micro_steps > 1 else 0)
+    pipeline = {}
+    if wl.per_bucket:
+        launches_per_step = L.num_buckets + 1
+        firsts = [a.elapsed_time(f) for (a, _), f in zip(ev, first_bucket_done)]
+        pipeline = {"pipeline": {"buckets": L.num_buckets, "streams": 2,
+                                 "first_bucket_ready_ms": statistics.median(firsts),
+                                 "note": "time from the step's start until the first bucket's "
+                                         "parameters are final (an all-gather could start)"}}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world_size,
         "steps": nsteps, "warmup": args.warmup, "ms_per_step": total_ms / nsteps,
@@ -457,6 +488,7 @@ def run_ours(args, wl):
                           "gbs": n_elems * 24 / (kernel_ms / 1e3) / 1e9,
                           "note": "master/m/v read and written in Grace memory over NVLink-C2C"}}
            if wl.offload_state else {}),
+        **pipeline,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line))

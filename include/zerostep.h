@@ -374,7 +374,7 @@ ZERO_API int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state
  *    reducing it twice (2 * N_d bytes read per element are replaced by 8).
  *  state_dev: device step state.  ws: device workspace of ws_bytes >=
  *    zero_workspace_bytes(layout->world).
- * Offload (next row f4): master, m and v (all six slots) may instead be
+ * Offload: master, m and v (all six slots) may instead be
  *  pinned host memory (cudaHostAlloc / cudaHostRegister) that the GPU reads
  *  and writes over the host link while gradients and parameters stay in
  *  device memory, as in ZeRO-Offload, where the optimizer state lives in CPU
@@ -391,6 +391,40 @@ ZERO_API int zero_step_fused(const void *const *grads, int grads_are_slices, zer
                              float *g_stage, const zero_adam_cfg *cfg,
                              zero_step_state *state_dev, void *ws, size_t ws_bytes,
                              zero_stream_t stream);
+
+/*
+ * The one-pass step (a2)-(a7) on buckets [first_bucket, first_bucket +
+ * n_buckets) of a layout, WITHOUT the commit (a8).  Call it once per range,
+ * so that every bucket of the layout is covered exactly once per step.  The
+ * ranges may go to different streams and run concurrently, since they touch
+ * disjoint elements.  After all of them, call zero_step_finalize(cfg,
+ * state_dev, 1, stream) on a stream ordered after every range.  The result
+ * is then bit for bit the zero_step_fused result.
+ * A range's half-precision parameters are final as soon as that range's work
+ * completes, so a caller can start that bucket's all-gather while later
+ * buckets are still being updated.  A NaN/Inf found in any range makes the
+ * commit skip the whole step, as the unused ping-pong slot is the only one
+ * written.  This is DeepSpeed's overlap of the optimizer step with the
+ * parameter all-gather ("DeepSpeed ZeRO", ZeRO Stage 1, 通信与计算重叠: start
+ * the all-gather of each updated part while the rest is still updating) over
+ * its constant-size buffers ("相关分析", Constant Size Buffer).
+ *  Arguments as zero_step_fused, except:
+ *  first_bucket, n_buckets: 0 <= first_bucket, first_bucket + n_buckets <=
+ *    layout->num_buckets (a layout without buckets has one bucket, the whole
+ *    vector).  n_buckets = 0 enqueues nothing.
+ *  There is no g_stage and no workspace: a clipped step needs the global norm
+ *    before any update, so cfg->max_grad_norm > 0 is ZERO_EINVAL.
+ * Every bucket must be processed before the commit, and none twice: after the
+ * commit, a bucket left out would hold the slot's older contents.  That is
+ * the caller's contract; the library does not track it.
+ */
+ZERO_API int zero_step_fused_buckets(const void *const *grads, int grads_are_slices,
+                                     zero_dtype dtype, const zero_layout *layout, int rank,
+                                     int64_t first_bucket, int64_t n_buckets,
+                                     float *const master[2], float *const m[2],
+                                     float *const v[2], void *const params[2],
+                                     const zero_adam_cfg *cfg, zero_step_state *state_dev,
+                                     zero_stream_t stream);
 
 #ifdef __cplusplus
 }

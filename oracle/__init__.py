@@ -460,7 +460,7 @@ def window_step(grads: Sequence[np.ndarray], dtype: int, cfg: AdamCfg, st: State
 
 
 # --------------------------------------------------------------------------
-# Gradient accumulation (next row f2)
+# Gradient accumulation
 # --------------------------------------------------------------------------
 
 def reduce_scatter_accumulate(grads: Sequence[np.ndarray], dtype: int, lay: Layout,

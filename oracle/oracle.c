@@ -161,7 +161,7 @@ void orc_reduce_sum(const uint16_t *const *grads, int world, int dtype, int64_t 
     }
 }
 
-/* Gradient accumulation over micro-steps (next row f2): acc[j] = acc[j] + r[j]
+/* Gradient accumulation over micro-steps: acc[j] = acc[j] + r[j]
  * in binary32, where r is one micro-step's reduce-scattered sum.  "DeepSpeed
  * ZeRO", "ZeRO-2 在梯度累积场景下的通信量": ZeRO-2 reduce-scatters after every
  * backward and accumulates its 1/N_d slice; the memory section of the same
@@ -174,7 +174,7 @@ void orc_accumulate(float *acc, const float *r, int64_t n)
 }
 
 /*
- * Step (a2) with the reduction itself in half precision (next row f3): the
+ * Step (a2) with the reduction itself in half precision: the
  * running sum is kept in the gradient's type and rounded to nearest even
  * after every addition, in ascending rank order from +0, as a half-precision
  * reduce-scatter produces it ("DeepSpeed ZeRO", ZeRO Stage 2: the fp32

@@ -76,6 +76,7 @@ class Workload:
     micro_steps: int = 1                 # gradient-accumulation micro-steps per step
     half_reduce: bool = False            # reduce in the gradients' half type, not fp32
     offload_state: bool = False          # master/m/v in pinned host memory
+    per_bucket: bool = False             # one launch per bucket on two streams, then the commit
 
     @property
     def numel(self) -> int:
@@ -159,5 +160,14 @@ OFFLOAD_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-offload", offload_state=Tr
 # slots of the full half-precision parameter vector).
 PROFILE_CFG4 = CFG4.replace(name="600M-shard-nd64-rank0-fp16", numels=(600_000_000,))
 
+# The 1.5B, 16-rank workload cut into 60 buckets of 25,000,064 elements (the
+# multiple of 16 x 8 nearest 25M): as one launch, and as one launch per
+# bucket alternating between two streams with one commit at the end (the
+# optimizer step whose finished buckets an all-gather can take while later
+# buckets update).
+BUCKET_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-bucket25M", bucket=25_000_064)
+PERBUCKET_CFG3 = BUCKET_CFG3.replace(name="flat-1.5B-nd16-fp16-bucket25M-perbucket",
+                                     per_bucket=True)
+
 BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, PROFILE_CFG4, ACCUM_CFG3, HALFRED_CFG3,
-                                     OFFLOAD_CFG3)}
+                                     OFFLOAD_CFG3, BUCKET_CFG3, PERBUCKET_CFG3)}

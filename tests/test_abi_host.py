@@ -35,7 +35,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(zs):
     names = declared_functions()
-    assert len(names) == 16, names
+    assert len(names) == 17, names
     so = ctypes.CDLL(zs._build.LIB)
     for n in names:
         assert hasattr(so, n), n
@@ -67,6 +67,30 @@ def test_host_alloc_arguments(zs):
     assert L.zero_host_alloc(64, None) == -1
     assert L.zero_host_free(None) == 0
     assert zs.host_empty(0, zs.torch_dtype(zs.F16)).numel() == 0
+
+
+def test_bucket_step_validates_before_launch(zs):
+    """zero_step_fused_buckets rejects a clipped config, ranges outside the
+    layout's buckets and aliased slots before anything is enqueued, and a
+    zero-bucket range enqueues nothing."""
+    lib = zs._abi.lib()
+    E = zs._abi
+    lay, _ = zs.zero_partition_layout([100_000, 3], 2, bucket_numel=2 * 8 * 1024)
+    assert lay.num_buckets == 7
+    fake = 1 << 20
+    g2 = (ctypes.c_void_p * 2)(fake, fake)
+    slots = (ctypes.c_void_p * 2)(fake, fake + 4096)
+    same = (ctypes.c_void_p * 2)(fake, fake)
+
+    def call(first, n, cfg=zs.adam_cfg(), w=slots):
+        return lib.zero_step_fused_buckets(g2, 0, 0, ctypes.byref(lay), -1, first, n, w, slots,
+                                           slots, slots, ctypes.byref(cfg), fake, None)
+
+    assert call(0, 1, zs.adam_cfg(max_grad_norm=1.0)) == E.EINVAL
+    for first, n in ((-1, 1), (0, -1), (7, 1), (6, 2), (0, 8), (1 << 62, 1 << 62)):
+        assert call(first, n) == E.EINVAL, (first, n)
+    assert call(0, 1, w=same) == E.EINVAL
+    assert call(3, 0) == E.OK and call(7, 0) == E.OK
 
 
 def test_structs_match_header(tmp_path, zs):

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from synth.workloads import CFG2, CFG3, CFG4, CFG5
+from synth.workloads import CFG2, CFG3, CFG4, CFG5, PERBUCKET_CFG3
 import zero_partitioned_mixed_step_gb300 as zs
 from zs_harness import (INF_BITS, SUMSQ_RTOL, assert_close, assert_half_close, half_bits,
                         lib_cfg, oracle_cfg)
@@ -161,6 +161,28 @@ def flat_of_local(lay, r, k, n):
     raise AssertionError("window outside the rank")
 
 
+def step_group(z, grads, wl):
+    """The step as the benchmark launches it: one fused call, or (per-bucket
+    workloads) one call per bucket alternating between two streams, then the
+    commit."""
+    if not wl.per_bucket:
+        z.step(grads)
+        return
+    s0 = torch.cuda.current_stream()
+    side = [torch.cuda.Stream(), torch.cuda.Stream()]
+    go = torch.cuda.Event()
+    go.record(s0)
+    for st in side:
+        st.wait_event(go)
+    for b in range(z.layout.num_buckets):
+        z.step_buckets(grads, b, 1, side[b % 2])
+    for st in side:
+        done = torch.cuda.Event()
+        done.record(st)
+        s0.wait_event(done)
+    z.commit(s0)
+
+
 def run_windowed(wl, steps, stage=None):
     grp = GpuGroup(wl, stage)
     lay, z = grp.lay, grp.z
@@ -180,7 +202,7 @@ def run_windowed(wl, steps, stage=None):
     for s in range(1, steps + 1):
         S = st.loss_scale
         grp.regen(s, S)
-        z.step(grp.grads)
+        step_group(z, grp.grads, wl)
         flag, sumsq = oracle.scan_scalars(grp.chunk, wl.dtype, lay, oracle.f32(1.0 / S),
                                           cfg.max_grad_norm > 0, openmp=True, ranks=ranks)
         for key, (w, m, v, h) in state.items():
@@ -230,6 +252,13 @@ def test_fullsize_1p5B_nd16_dynamic():
     run skips twice)."""
     st = run_windowed(CFG3.replace(inject_every=2), steps=5)
     assert st.skipped == 2 and st.t == 3 and st.loss_scale == 1024.0
+
+
+def test_fullsize_1p5B_nd16_per_bucket():
+    """The 1.5B, 16-rank workload in 60 buckets of 25,000,064 elements, run
+    as one launch per bucket on two streams and one commit; +Inf in step 2."""
+    st = run_windowed(PERBUCKET_CFG3.replace(inject_every=2), steps=3)
+    assert st.skipped == 1 and st.t == 2
 
 
 def test_fullsize_7p5B_rank0_nd64():

@@ -28,7 +28,8 @@ __all__ = [
     "adam_cfg", "new_state", "read_state", "state_field_ptr", "zero_partition_layout",
     "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
     "zero_grad_norm", "zero_grad_norm_noalloc", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
-    "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated", "host_empty",
+    "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated", "zero_step_fused_buckets",
+    "host_empty",
 ]
 
 _TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
@@ -223,6 +224,23 @@ def zero_step_fused(grads: Sequence[torch.Tensor], layout: Layout,
                                 ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def zero_step_fused_buckets(grads: Sequence[torch.Tensor], layout: Layout, first_bucket: int,
+                            n_buckets: int, master: Sequence[torch.Tensor],
+                            m: Sequence[torch.Tensor], v: Sequence[torch.Tensor],
+                            params: Sequence[torch.Tensor], cfg: AdamCfg, state: torch.Tensor,
+                            rank: int = -1, grads_are_slices: bool = False, stream=None,
+                            half_reduce: bool = False) -> None:
+    """Steps (a2)-(a7) of the one-pass step on buckets [first_bucket,
+    first_bucket + n_buckets), without the commit; zero_step_finalize(cfg,
+    state, flip_slot=True) commits once every bucket has been processed."""
+    check("zero_step_fused_buckets",
+          lib().zero_step_fused_buckets(_ptr_array(grads), int(grads_are_slices),
+                                        _grad_code(grads, half_reduce), ctypes.byref(layout),
+                                        rank, first_bucket, n_buckets, _state_array(master),
+                                        _state_array(m), _state_array(v), _ptr_array(params),
+                                        ctypes.byref(cfg), _dev_ptr(state), _stream(stream)))
+
+
 def zero_reduce_scatter_accumulate(grads: Sequence[torch.Tensor], layout: Layout,
                                    acc: torch.Tensor, add: bool, rank: int = -1,
                                    grads_are_slices: bool = False, stream=None,
@@ -323,6 +341,17 @@ class ZeroStep:
         zero_step_fused(grads, self.layout, self.master, self.m, self.v, self.params, self.cfg,
                         self.state, self.ws, self.rank, self.g_stage, self.grads_are_slices,
                         stream, self.half_reduce)
+
+    def step_buckets(self, grads: Sequence[torch.Tensor], first_bucket: int, n_buckets: int,
+                     stream=None) -> None:
+        """The one-pass step on a range of buckets, without the commit."""
+        zero_step_fused_buckets(grads, self.layout, first_bucket, n_buckets, self.master,
+                                self.m, self.v, self.params, self.cfg, self.state, self.rank,
+                                self.grads_are_slices, stream, self.half_reduce)
+
+    def commit(self, stream=None) -> None:
+        """End a step run bucket by bucket: commit, or skip on NaN/Inf."""
+        zero_step_finalize(self.cfg, self.state, True, stream)
 
     def accumulate(self, grads: Sequence[torch.Tensor], add: bool, stream=None) -> None:
         """One micro-step into the group's fp32 gradient accumulator (allocated

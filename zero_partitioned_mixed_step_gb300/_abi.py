@@ -69,6 +69,8 @@ SIGNATURES = {
     "zero_step_fused": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _P, _P, _P, _P, _P,
                          ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P], _I),
     "zero_reduce_scatter_accumulate": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _P, _I, _P], _I),
+    "zero_step_fused_buckets": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _I64, _I64, _P, _P, _P,
+                                 _P, ctypes.POINTER(AdamCfg), _P, _P], _I),
     "zero_step_fused_accumulated": ([_P, _I, ctypes.POINTER(Layout), _I, _P, _P, _P, _P,
                                      ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P], _I),
 }

@@ -382,14 +382,12 @@ int state_residence(float *const master[2], float *const m[2], float *const v[2]
     return first < 0 ? ZERO_EINVAL : first;
 }
 
-// Checks of the ping-pong slots, stage, state and workspace shared by the
-// fused entry points.
-int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *const master[2],
-                float *const m[2], float *const v[2], void *const params[2], const float *stage,
-                bool stage_allowed, const zero_step_state *state_dev, const void *ws,
-                size_t ws_bytes)
+// Checks of the ping-pong slots and the state shared by the fused entry points.
+int check_pingpong(const zero_layout *layout, const zero_adam_cfg *cfg, float *const master[2],
+                   float *const m[2], float *const v[2], void *const params[2],
+                   const zero_step_state *state_dev)
 {
-    if (!master || !m || !v || !params || !state_dev || !ws)
+    if (!master || !m || !v || !params || !state_dev)
         return ZERO_EINVAL;
     const bool clip = cfg->max_grad_norm > 0.0;
     const bool empty = layout->padded_numel == 0;  // nothing to read or write
@@ -402,10 +400,25 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
     if (!clip && !empty &&
         (master[0] == master[1] || m[0] == m[1] || v[0] == v[1] || params[0] == params[1]))
         return ZERO_EINVAL;  // a one-pass step needs distinct slots to be able to skip
+    if (reinterpret_cast<uintptr_t>(state_dev) & 7u)
+        return ZERO_EALIGN;
+    return ZERO_OK;
+}
+
+// check_pingpong, plus the stage and the workspace.
+int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *const master[2],
+                float *const m[2], float *const v[2], void *const params[2], const float *stage,
+                bool stage_allowed, const zero_step_state *state_dev, const void *ws,
+                size_t ws_bytes)
+{
+    if (!ws)
+        return ZERO_EINVAL;
+    const int rc = check_pingpong(layout, cfg, master, m, v, params, state_dev);
+    if (rc)
+        return rc;
     if (stage && !stage_allowed)
         return ZERO_EINVAL;
-    if ((stage && !aligned32(stage)) || !aligned16(ws) ||
-        (reinterpret_cast<uintptr_t>(state_dev) & 7u))
+    if ((stage && !aligned32(stage)) || !aligned16(ws))
         return ZERO_EALIGN;
     if (ws_bytes < zero_workspace_bytes(layout->world))
         return ZERO_ESPACE;
@@ -477,8 +490,10 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
                             : launch_staged_w<ZERO_F16, kStagedWorld>(p, stream);
 }
 
-// One step (one or two passes, then the finalize) in the given modes.
-int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream)
+// One step (one or two passes, then the finalize unless commit is false) in
+// the given modes.
+int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream,
+             bool commit = true)
 {
     int rc, gx = 1;
     if (a.lay->padded_numel > 0) {
@@ -498,7 +513,7 @@ int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStr
                 return rc;
         }
     }
-    return launch_finalize(a.cfg, a.state, 1, stream);
+    return commit ? launch_finalize(a.cfg, a.state, 1, stream) : ZERO_OK;
 }
 
 }  // namespace zs
@@ -597,4 +612,59 @@ extern "C" int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
     PassArgs a{nullptr, 0, dtype, layout, rank, cfg, state_dev,
                master, m, v, params, const_cast<float *>(acc), partials, 0};
     return run_step(a, clip, M_ACC_FUSED, M_ACC_PASS1, M_ACC_PASS2, stream);
+}
+
+extern "C" int zero_step_fused_buckets(const void *const *grads, int grads_are_slices,
+                                       zero_dtype dtype, const zero_layout *layout, int rank,
+                                       int64_t first_bucket, int64_t n_buckets,
+                                       float *const master[2], float *const m[2],
+                                       float *const v[2], void *const params[2],
+                                       const zero_adam_cfg *cfg, zero_step_state *state_dev,
+                                       zero_stream_t stream)
+{
+    int rc = check_grads(grads, grads_are_slices, dtype, layout, rank);
+    if (rc)
+        return rc;
+    if ((rc = check_cfg(cfg)))
+        return rc;
+    const zero_layout &L = *layout;
+    if (cfg->max_grad_norm > 0.0 || first_bucket < 0 || n_buckets < 0 ||
+        first_bucket > L.num_buckets - n_buckets)
+        return ZERO_EINVAL;
+    if ((rc = check_pingpong(layout, cfg, master, m, v, params, state_dev)))
+        return rc;
+    if (n_buckets == 0 || L.padded_numel == 0)
+        return ZERO_OK;
+    // The buckets of the range as a layout of their own; the buffers are
+    // offset to the range's first element.  Each bucket's rank slices lie
+    // inside it, so the range is a self-contained bucketed vector.
+    zero_layout S = L;
+    int64_t flat_off = 0, owned_off = 0;
+    if (L.bucket_numel > 0) {
+        const int64_t end = first_bucket + n_buckets;
+        S.num_buckets = n_buckets;
+        S.last_slice_numel = end == L.num_buckets ? L.last_slice_numel : L.slice_numel;
+        S.owned_numel = (n_buckets - 1) * L.slice_numel + S.last_slice_numel;
+        S.padded_numel = S.owned_numel * L.world;
+        S.numel = S.flat_numel = S.padded_numel;
+        flat_off = first_bucket * L.bucket_numel;
+        owned_off = first_bucket * L.slice_numel;
+    }
+    const int64_t state_off = rank < 0 ? flat_off : owned_off;
+    const int64_t grad_off = grads_are_slices ? owned_off : flat_off;
+    const void *g[ZERO_MAX_WORLD];
+    for (int q = 0; q < L.world; ++q)
+        g[q] = static_cast<const uint16_t *>(grads[q]) + grad_off;
+    float *w2[2] = {master[0] + state_off, master[1] + state_off};
+    float *m2[2] = {m[0] + state_off, m[1] + state_off};
+    float *v2[2] = {v[0] + state_off, v[1] + state_off};
+    void *p2[2] = {static_cast<uint16_t *>(params[0]) + flat_off,
+                   static_cast<uint16_t *>(params[1]) + flat_off};
+    PassArgs a{g, grads_are_slices, dtype, &S, rank, cfg, state_dev,
+               w2, m2, v2, p2, nullptr, nullptr, 0};
+    const int where = state_residence(w2, m2, v2);
+    if (where < 0)
+        return ZERO_EINVAL;  // mixed residence
+    a.host_state = where == 1;
+    return run_step(a, false, M_FUSED, M_PASS1, M_PASS2_RECOMPUTE, stream, false);
 }
