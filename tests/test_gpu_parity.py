@@ -77,6 +77,13 @@ EDGE = {
     "three-ranks-generic": CFG1.replace(numels=(100_003, 17), world=3, steps=3,
                                         inject_at=((2, 1, 50_000),)),
     "hundred-ranks": CFG1.replace(numels=(100 * 640 + 8,), world=100, steps=2, inject_at=()),
+    # the largest group the ABI accepts; the Inf is in the last rank's gradient, at the
+    # vector's last element (owned by rank 682)
+    "max-world-1024": CFG1.replace(numels=(1024 * 128 + 8,), world=1024, steps=2,
+                                   inject_at=((2, 1023, 1024 * 128 + 7),)),
+    # zero gradients: the moments stay zero and only the decoupled decay moves w
+    "zero-gradients": CFG1.replace(numels=(40_000,), world=4, grad_sigma=0.0, steps=2,
+                                   inject_at=()),
     "psi-below-world": CFG1.replace(numels=(5,), world=8, steps=2, inject_at=()),
     "tiny-tensors-gaps": CFG2.replace(numels=(1, 2, 3, 65, 127, 4096, 7), world=4, steps=3),
     "bf16-dynamic": CFG3.replace(numels=(200_000,), world=8, dtype=synth.BF16, steps=4,
