@@ -452,7 +452,7 @@ def run_ours(args, wl):
     peak = peaks["hbm_gbs"]
     traffic = recorded_traffic(wl.name)
     rate, threads, desc = oracle_sample_rate(wl)
-    launches_per_step = (4 if clip else 2) + (wl.micro_steps if wl.micro_steps > 1 else 0)
+    launches_per_step = (3 if clip else 2) + (wl.micro_steps if wl.micro_steps > 1 else 0)
     pipeline = {}
     if wl.per_bucket:
         launches_per_step = L.num_buckets + 1

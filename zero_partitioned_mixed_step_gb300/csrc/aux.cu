@@ -130,12 +130,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ double row_sum[ZERO_MAX_WORLD];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int r = warp; r < gy; r += kThreads / 32) {
-        double x = 0.0;
-        for (int i = lane; i < gx; i += 32)
-            x = __dadd_rn(x, partials[(int64_t)r * gx + i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+        const double x = warp_fixed_sum(partials + (int64_t)r * gx, gx);
         if (lane == 0)
             row_sum[r] = x;
     }
@@ -150,8 +145,7 @@ __global__ void __launch_bounds__(kThreads)
     if (st && !st->found_inf) {
         st->sumsq = total;
         if (max_norm > 0.0)
-            st->clip_coef = __double2float_rn(
-                fmin(1.0, __ddiv_rn(max_norm, __dadd_rn(__dsqrt_rn(total), 1e-6))));
+            st->clip_coef = clip_coefficient(total, max_norm);
     }
 }
 
@@ -220,7 +214,7 @@ __global__ void __launch_bounds__(kThreads)
 {
     __shared__ Scalars sh;
     if (threadIdx.x == 0)
-        compute_scalars(cfg, st, sh);
+        compute_scalars(cfg, st, st->sumsq, sh);
     __syncthreads();
     const Scalars s = sh;
     if (s.skip)

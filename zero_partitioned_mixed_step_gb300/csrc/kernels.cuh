@@ -34,6 +34,15 @@ __device__ __forceinline__ uint64_t evict_first_policy()
     return pol;
 }
 
+// The same hint the other way round, for data that a second pass reads again
+// while it can still be in L2 (the tail of a clipped step's first pass).
+__device__ __forceinline__ uint64_t evict_last_policy()
+{
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 16 bytes of one rank's gradient (read-only during the kernel).
 __device__ __forceinline__ uint4 ld_stream(const uint16_t *p, uint64_t pol)
 {
@@ -67,6 +76,39 @@ __device__ __forceinline__ void store8(float *p, const float x[8])
           "r"(__float_as_uint(x[2])), "r"(__float_as_uint(x[3])), "r"(__float_as_uint(x[4])),
           "r"(__float_as_uint(x[5])), "r"(__float_as_uint(x[6])), "r"(__float_as_uint(x[7]))
         : "memory");
+}
+
+// load8 / store8 marked evict-last in L2.
+__device__ __forceinline__ void load8_keep(const float *p, float x[8])
+{
+    uint32_t u[8];
+    asm("ld.global.L1::no_allocate.L2::evict_last.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7])
+        : "l"(p));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        x[i] = __uint_as_float(u[i]);
+}
+
+__device__ __forceinline__ void store8_keep(float *p, const float x[8])
+{
+    asm volatile(
+        "st.global.L1::no_allocate.L2::evict_last.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+        :
+        : "l"(p), "r"(__float_as_uint(x[0])), "r"(__float_as_uint(x[1])),
+          "r"(__float_as_uint(x[2])), "r"(__float_as_uint(x[3])), "r"(__float_as_uint(x[4])),
+          "r"(__float_as_uint(x[5])), "r"(__float_as_uint(x[6])), "r"(__float_as_uint(x[7]))
+        : "memory");
+}
+
+// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// its contents become undefined.  Used on a scratch line whose last reader
+// has read it, so that a dirty line the step no longer needs costs no DRAM
+// write.
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
 // The same 8 fp32 values in pinned host memory, reached over the host link:
@@ -306,9 +348,17 @@ struct Scalars {
     int32_t adamw, clip, skip;
 };
 
-// Scalars of step t + 1 from the state at the start of the step.
+// Clip coefficient min(1, max_norm / (sqrt(sumsq) + 1e-6)), binary64 rounded
+// once to binary32.
+__device__ __forceinline__ float clip_coefficient(double sumsq, double max_norm)
+{
+    return __double2float_rn(fmin(1.0, __ddiv_rn(max_norm, __dadd_rn(__dsqrt_rn(sumsq), 1e-6))));
+}
+
+// Scalars of step t + 1 from the state at the start of the step; sumsq is the
+// step's global sum of squares (read only when clipping).
 __device__ __forceinline__ void compute_scalars(const CfgDev &c, const zero_step_state *st,
-                                                Scalars &s)
+                                                double sumsq, Scalars &s)
 {
     const double bp1 = __dmul_rn(st->beta1_pow, c.beta1);
     const double bp2 = __dmul_rn(st->beta2_pow, c.beta2);
@@ -329,11 +379,7 @@ __device__ __forceinline__ void compute_scalars(const CfgDev &c, const zero_step
     s.adamw = c.adamw;
     s.inv_s = __fdiv_rn(1.0f, st->loss_scale);
     s.clip = c.max_norm > 0.0;
-    s.coef = 1.0f;
-    if (s.clip) {
-        const double n = __dsqrt_rn(st->sumsq);
-        s.coef = __double2float_rn(fmin(1.0, __ddiv_rn(c.max_norm, __dadd_rn(n, 1e-6))));
-    }
+    s.coef = s.clip ? clip_coefficient(sumsq, c.max_norm) : 1.0f;
     s.skip = st->found_inf;
 }
 
@@ -420,6 +466,32 @@ __device__ __forceinline__ double block_sum(double x)
             total = __dadd_rn(total, warp_sums[w]);
     }
     return total;
+}
+
+// Sum of n per-CTA partials in a fixed order, the result valid in every lane
+// of the calling (whole) warp: lane l adds p[l], p[l + 32], p[l + 64] ... in
+// index order from +0 (the loads are issued eight at a time; the order of
+// the additions does not change), then a fixed butterfly combines the lanes.
+__device__ __forceinline__ double warp_fixed_sum(const double *p, int n)
+{
+    const int lane = threadIdx.x & 31;
+    double x = 0.0;
+    int i = lane;
+    for (; i + 7 * 32 < n; i += 8 * 32) {
+        double y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            y[j] = p[i + 32 * j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            x = __dadd_rn(x, y[j]);
+    }
+    for (; i < n; i += 32)
+        x = __dadd_rn(x, p[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
 }
 
 // Report a non-finite gradient of this warp once.

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
     const int nst = p.stages;
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
     if (tid == 0) {
-        compute_scalars(p.cfg, p.state, sh);
+        compute_scalars(p.cfg, p.state, p.state->sumsq, sh);
         sh_cur = p.state->cur;
         abort_flag = 0;
         for (int st = 0; st < nst; ++st) {

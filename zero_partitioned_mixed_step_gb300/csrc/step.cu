@@ -11,7 +11,10 @@
 //   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, per-CTA
 //              sums of squares, optionally keep g in a staging buffer.
 //   PASS2_*    (a5 clip)-(a7) of a clipped step, skipped when pass 1 flagged
-//              an overflow; g is reduced again or read from the stage.
+//              an overflow; every CTA first reduces pass 1's per-CTA sums of
+//              squares in one fixed order; g is reduced again or read from
+//              the stage.  It walks the units backwards, starting on the
+//              first pass's last units, whose data pass 1 left in L2.
 //   RS         (a2) alone: the reduced fp32 gradient.
 //   RS_ACC     (a2) into an fp32 accumulator (gradient accumulation).
 //   ACC_*      the step with the gradient read from an fp32 accumulator (the
@@ -57,8 +60,18 @@ struct StepParams {
     float *wo0, *wo1, *mo0, *mo1, *vo0, *vo1;   // ping-pong slots (writes)
     uint16_t *par0, *par1;                      // parameter buffer slots
     float *stage;      // PASS1 output / PASS2_STAGED input / RS output / accumulator
-    double *partials;  // PASS1: one per CTA
+    double *partials;  // PASS1: one per CTA; second passes reduce them
+    int32_t n_partials;  // second passes: CTAs of the first pass
     int32_t add;       // RS_ACC: add to the accumulator (else overwrite it)
+    // Clipped steps: the first pass marks what it reads or writes for units
+    // u >= keep_from evict-last in L2 (the stage it writes, else the
+    // accumulator or the gradients it reads), and the second pass walks the
+    // units backwards, so it starts on what is still in L2.  keep_from is a
+    // multiple of 4 (= units when nothing is kept).  discard: the second pass
+    // drops the stage's kept lines from L2 after reading them (the stage is
+    // 128-byte aligned), so they are never written back to DRAM.
+    int64_t keep_from;
+    int32_t discard;
 };
 
 // HOST_STATE: master, m and v live in pinned host memory (offload).  Its
@@ -75,20 +88,45 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
     __shared__ int sh_cur;
     Scalars s{};
     int cur = 0;
+    const View &vw = p.view;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
     if constexpr (!reduces_only(MODE)) {
-        if (threadIdx.x == 0) {
-            compute_scalars(p.cfg, p.state, sh);
+        if constexpr (second_pass(MODE)) {
+            // The global sum of squares, reduced by every CTA from the first
+            // pass's per-CTA partials in one fixed order (all CTAs get the
+            // same bits); CTA 0 publishes it in the state.
+            if (threadIdx.x < 32) {
+                const double x = warp_fixed_sum(p.partials, p.n_partials);
+                if (threadIdx.x == 0) {
+                    const double total = __dadd_rn(0.0, x);
+                    compute_scalars(p.cfg, p.state, total, sh);
+                    sh_cur = p.state->cur;
+                    if (blockIdx.x == 0 && !sh.skip) {
+                        p.state->sumsq = total;
+                        p.state->clip_coef = sh.coef;
+                    }
+                }
+            }
+        } else if (threadIdx.x == 0) {
+            compute_scalars(p.cfg, p.state, p.state->sumsq, sh);
             sh_cur = p.state->cur;
         }
         __syncthreads();
         s = sh;
         cur = sh_cur;
         if constexpr (second_pass(MODE)) {
-            if (s.skip)
-                return;  // the whole step is skipped: write nothing
+            if (s.skip) {  // the whole step is skipped: write nothing
+                if constexpr (MODE == M_PASS2_STAGED) {
+                    if (p.discard)  // the kept stage lines are not needed either
+                        for (int64_t u = p.keep_from +
+                                         4 * ((int64_t)blockIdx.x * kThreads + threadIdx.x);
+                             u + 4 <= vw.units; u += 4 * stride)
+                            discard_l2_line(p.stage + u * kUnit);
+                }
+                return;
+            }
         }
     }
-    const View &vw = p.view;
     const float *w_src = cur ? p.w1 : p.w0;
     const float *m_src = cur ? p.m1 : p.m0;
     const float *v_src = cur ? p.v1 : p.v0;
@@ -98,12 +136,16 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
     uint16_t *out = cur ? p.par0 : p.par1;
 
     const uint64_t pol = evict_first_policy();
+    uint64_t keep_pol = pol;
+    if constexpr (sums_squares(MODE))
+        keep_pol = evict_last_policy();
     bool bad = false;
     SumSq ss;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < vw.units; u += stride) {
+    // One unit: the whole per-element work of the mode.
+    auto unit = [&](int64_t u) {
         int64_t f, si, gi;
         locate<ALL>(vw, u, f, si, gi);
+        const bool keep = sums_squares(MODE) && u >= p.keep_from;
         // The state loads are issued before the gradient loads, so that a
         // unit's whole input is in flight at once (1.3 % faster on the 64-rank
         // shard, no change at 16 ranks).
@@ -123,15 +165,20 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
         if constexpr (MODE == M_PASS2_STAGED) {
             load8(p.stage + si, g);  // already unscaled by pass 1
         } else if constexpr (reads_accumulator(MODE)) {
-            load8(p.stage + si, g);
+            if (keep)
+                load8_keep(p.stage + si, g);
+            else
+                load8(p.stage + si, g);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 g[i] = __fmul_rn(g[i], s.inv_s);
         } else {
-            reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g, pol);
+            // a first pass that will reduce again keeps its tail's gradients
+            const bool keep_grads = keep && MODE == M_PASS1 && !p.stage;
+            reduce_unit<DT, W, MAXW>(p.grads, vw.world, gi, g, keep_grads ? keep_pol : pol);
             if constexpr (MODE == M_RS) {
                 store8(p.stage + si, g);
-                continue;
+                return;
             }
             if constexpr (MODE == M_RS_ACC) {
                 if (p.add) {
@@ -142,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
                         g[i] = __fadd_rn(a[i], g[i]);
                 }
                 store8(p.stage + si, g);
-                continue;
+                return;
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -155,9 +202,13 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
         }
         if constexpr (sums_squares(MODE)) {
             ss.add8(g);
-            if (MODE == M_PASS1 && p.stage)
-                store8(p.stage + si, g);
-            continue;
+            if (MODE == M_PASS1 && p.stage) {
+                if (keep)
+                    store8_keep(p.stage + si, g);
+                else
+                    store8(p.stage + si, g);
+            }
+            return;
         }
         if constexpr (second_pass(MODE)) {
             if (s.coef < 1.0f) {
@@ -177,6 +228,31 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
             store8(v_dst + si, v);
         }
         st_half8(out + f, pack_half8<DT>(w), pol);
+    };
+
+    const int64_t base = (int64_t)blockIdx.x * kThreads;
+    if constexpr (second_pass(MODE)) {
+        // Backwards over the grid-stride sequence: the units the first pass
+        // reached last come first, while their lines can still be in L2.
+        if (base < vw.units) {
+            for (int64_t k = (vw.units - 1 - base) / stride; k >= 0; --k) {
+                const int64_t first = base + k * stride;  // the CTA's first unit this round
+                const int64_t u = first + threadIdx.x;
+                if (u < vw.units)
+                    unit(u);
+                if constexpr (MODE == M_PASS2_STAGED) {
+                    if (p.discard && first + kThreads > p.keep_from) {  // uniform in the CTA
+                        // lanes 4j .. 4j + 3 read the four units of one line
+                        __syncwarp();
+                        if ((threadIdx.x & 3) == 0 && u >= p.keep_from && u + 4 <= vw.units)
+                            discard_l2_line(p.stage + u * kUnit);
+                    }
+                }
+            }
+        }
+    } else {
+        for (int64_t u = base + threadIdx.x; u < vw.units; u += stride)
+            unit(u);
     }
     if constexpr (flags_overflow(MODE))
         flag_nonfinite(bad, &p.state->found_inf);
@@ -278,6 +354,9 @@ struct PassArgs {
     double *partials;
     int add;
     bool host_state = false;  // master/m/v in pinned host memory (one-pass step only)
+    int n_partials = 0;       // second passes: CTAs of the first pass
+    int64_t keep_from = INT64_MAX;  // clipped steps: see StepParams
+    bool discard = false;
 };
 
 // The one-pass step with the optimizer state in pinned host memory: one
@@ -334,7 +413,10 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
     }
     p.stage = a.stage;
     p.partials = a.partials;
+    p.n_partials = a.n_partials;
     p.add = a.add;
+    p.keep_from = a.keep_from < v.units ? a.keep_from : v.units;
+    p.discard = a.discard && p.keep_from < v.units ? 1 : 0;
     if (a.host_state)
         return dispatch_host_state<MAXW>(p, a.dtype, stream, gx);
     return dispatch<MAXW>(p, a.dtype, mode, stream, gx);
@@ -500,13 +582,23 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
                             : launch_staged_w<ZERO_F16, kStagedWorld>(p, stream);
 }
 
+// Bytes of a clipped step's first-pass data (the stage it writes, else the
+// accumulator or the gradients it reads) left in L2 for the second pass: about
+// half of GB300's 126 MB L2.
+#ifndef ZS_KEEP_MB
+#define ZS_KEEP_MB 64
+#endif
+constexpr int64_t kKeepBytes = (int64_t)ZS_KEEP_MB << 20;
+
 // One step (one or two passes, then the finalize unless commit is false) in
-// the given modes.
+// the given modes.  A clipped step's second pass reduces the first pass's
+// per-CTA sums of squares itself (there is no separate norm kernel).
 int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream,
              bool commit = true)
 {
     int rc, gx = 1;
-    if (a.lay->padded_numel > 0) {
+    const zero_layout &L = *a.lay;
+    if (L.padded_numel > 0) {
         if (!clip) {
             rc = one_pass == M_FUSED ? launch_staged(a, stream) : 1;
             if (rc == 1)
@@ -514,11 +606,17 @@ int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStr
             if (rc)
                 return rc;
         } else {
+            const int64_t units = (a.rank < 0 ? L.padded_numel : L.owned_numel) / kUnit;
+            const bool regrads = pass1 == M_PASS1 && !a.stage;  // pass 2 reduces again
+            const int64_t kept = kKeepBytes / (regrads ? 2 * kUnit * (int64_t)L.world : 4 * kUnit);
+            int64_t from = units > kept ? units - kept : 0;
+            from = (from + 3) / 4 * 4;
+            a.keep_from = from < units ? from : units;
+            a.discard = a.stage && pass2 == M_PASS2_STAGED &&
+                        (reinterpret_cast<uintptr_t>(a.stage) & 127u) == 0;
             if ((rc = run(a, pass1, stream, &gx)))
                 return rc;
-            if ((rc = launch_norm_finalize(a.partials, gx, 1, a.cfg->max_grad_norm, a.state,
-                                           nullptr, stream)))
-                return rc;
+            a.n_partials = gx;
             if ((rc = run(a, pass2, stream, &gx)))
                 return rc;
         }
