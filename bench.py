@@ -452,7 +452,9 @@ def run_ours(args, wl):
     peak = peaks["hbm_gbs"]
     traffic = recorded_traffic(wl.name)
     rate, threads, desc = oracle_sample_rate(wl)
-    launches_per_step = (3 if clip else 2) + (wl.micro_steps if wl.micro_steps > 1 else 0)
+    # the step's last kernel also ends the step: one launch per pass, plus one
+    # per accumulated micro-step
+    launches_per_step = (2 if clip else 1) + (wl.micro_steps if wl.micro_steps > 1 else 0)
     pipeline = {}
     if wl.per_bucket:
         launches_per_step = L.num_buckets + 1

@@ -157,7 +157,8 @@ typedef struct {
  * Step state, DEVICE-resident (64 bytes, 8-byte aligned), owned by the
  * caller.  Initialise a host copy with zero_state_init and copy it to the
  * device.  The kernels read it at the start of a step and zero_step_finalize
- * (or zero_step_fused) updates it at the end.
+ * (or the last kernel of zero_step_fused / zero_step_fused_accumulated)
+ * updates it at the end.
  */
 typedef struct {
     int64_t t;          /* committed (not skipped) steps */
@@ -168,7 +169,10 @@ typedef struct {
     float clip_coef;    /* clip coefficient of the last clipped step */
     int32_t good_steps; /* good steps since the last overflow or growth */
     int32_t overflow;   /* 1 if the last step was skipped */
-    int32_t found_inf;  /* OR of the non-finite flags of the step in progress */
+    int32_t found_inf;  /* bit 0: OR of the non-finite flags of the step in progress;
+                           while the last kernel of a fused step runs, the bits above
+                           count its finished CTAs (the last one ends the step); 0
+                           between steps */
     int32_t cur;        /* ping-pong slot (0/1) holding the current master/m/v/params */
     int32_t skipped;    /* number of skipped steps */
     int32_t error;      /* nonzero if a kernel gave up waiting for its own memory copies

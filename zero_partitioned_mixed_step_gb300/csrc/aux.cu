@@ -78,44 +78,16 @@ int target_ctas(const void *kernel)
 
 // ------------------------------------------------------------------ end of step
 
-struct FinCfg {
-    double beta1, beta2, backoff, growth, min_scale;
-    int32_t dynamic, interval;
-};
-
 __global__ void finalize_kernel(FinCfg c, zero_step_state *st, int flip)
 {
     if (threadIdx.x != 0 || blockIdx.x != 0)
         return;
-    if (st->found_inf) {
-        st->overflow = 1;
-        st->skipped += 1;
-        if (c.dynamic) {
-            const double s = __dmul_rn((double)st->loss_scale, c.backoff);
-            st->loss_scale = __double2float_rn(s > c.min_scale ? s : c.min_scale);
-            st->good_steps = 0;
-        }
-    } else {
-        st->overflow = 0;
-        st->t += 1;
-        st->beta1_pow = __dmul_rn(st->beta1_pow, c.beta1);
-        st->beta2_pow = __dmul_rn(st->beta2_pow, c.beta2);
-        if (flip)
-            st->cur ^= 1;
-        st->good_steps += 1;
-        if (c.dynamic && st->good_steps == c.interval) {
-            st->loss_scale = __double2float_rn(__dmul_rn((double)st->loss_scale, c.growth));
-            st->good_steps = 0;
-        }
-    }
-    st->found_inf = 0;
+    end_step(c, st, flip, st->found_inf & 1);
 }
 
 int launch_finalize(const zero_adam_cfg *cfg, zero_step_state *state, int flip, cudaStream_t s)
 {
-    FinCfg c{cfg->beta1, cfg->beta2, cfg->backoff, cfg->growth, cfg->min_scale,
-             cfg->dynamic_scale ? 1 : 0, cfg->growth_interval};
-    finalize_kernel<<<1, 32, 0, s>>>(c, state, flip);
+    finalize_kernel<<<1, 32, 0, s>>>(fin_cfg(*cfg), state, flip);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
@@ -142,7 +114,7 @@ __global__ void __launch_bounds__(kThreads)
         total = __dadd_rn(total, row_sum[r]);
     if (out)
         *out = total;
-    if (st && !st->found_inf) {
+    if (st && !(st->found_inf & 1)) {
         st->sumsq = total;
         if (max_norm > 0.0)
             st->clip_coef = clip_coefficient(total, max_norm);

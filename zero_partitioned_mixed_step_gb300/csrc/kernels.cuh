@@ -380,7 +380,73 @@ __device__ __forceinline__ void compute_scalars(const CfgDev &c, const zero_step
     s.inv_s = __fdiv_rn(1.0f, st->loss_scale);
     s.clip = c.max_norm > 0.0;
     s.coef = s.clip ? clip_coefficient(sumsq, c.max_norm) : 1.0f;
-    s.skip = st->found_inf;
+    s.skip = st->found_inf & 1;
+}
+
+// ------------------------------------------------------------------ end of step
+
+// What ending a step needs from the optimizer configuration.
+struct FinCfg {
+    double beta1, beta2, backoff, growth, min_scale;
+    int32_t dynamic, interval;
+};
+
+inline FinCfg fin_cfg(const zero_adam_cfg &c)
+{
+    return FinCfg{c.beta1, c.beta2, c.backoff, c.growth, c.min_scale, c.dynamic_scale ? 1 : 0,
+                  c.growth_interval};
+}
+
+// Step (a8) on the device state, one thread: skip (found = 1: count it, back
+// the dynamic loss scale off) or commit (t + 1, beta powers, slot flip, good
+// steps and loss-scale growth); found_inf is cleared either way.
+__device__ __forceinline__ void end_step(const FinCfg &c, zero_step_state *st, int flip,
+                                         int found)
+{
+    if (found) {
+        st->overflow = 1;
+        st->skipped += 1;
+        if (c.dynamic) {
+            const double s = __dmul_rn((double)st->loss_scale, c.backoff);
+            st->loss_scale = __double2float_rn(s > c.min_scale ? s : c.min_scale);
+            st->good_steps = 0;
+        }
+    } else {
+        st->overflow = 0;
+        st->t += 1;
+        st->beta1_pow = __dmul_rn(st->beta1_pow, c.beta1);
+        st->beta2_pow = __dmul_rn(st->beta2_pow, c.beta2);
+        if (flip)
+            st->cur ^= 1;
+        st->good_steps += 1;
+        if (c.dynamic && st->good_steps == c.interval) {
+            st->loss_scale = __double2float_rn(__dmul_rn((double)st->loss_scale, c.growth));
+            st->good_steps = 0;
+        }
+    }
+    st->found_inf = 0;
+}
+
+// The end of the step's last kernel, called by every thread of every CTA:
+// the step is ended by the CTA that finishes last, so no separate launch is
+// needed.  Bit 0 of found_inf is the step's non-finite flag; while the kernel
+// runs, the bits above count its CTAs that are done (found_inf is 0 between
+// steps, and end_step clears it).  A CTA's flag updates come before its count
+// (barrier, then a fence), and all updates are atomics on the one word, so
+// the CTA whose addition completes the count sees every CTA's flag in the old
+// value; all CTAs read the state they need when they start, before they
+// count themselves.
+__device__ __forceinline__ void arrive_and_end_step(const FinCfg &c, zero_step_state *st)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int32_t old = atomicAdd(&st->found_inf, 2);
+        if ((old >> 1) == (int32_t)gridDim.x - 1) {
+            __threadfence();
+            end_step(c, st, 1, old & 1);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ Adam

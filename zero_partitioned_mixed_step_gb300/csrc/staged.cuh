@@ -21,7 +21,8 @@
 // times without completion records the error in the step state, marks the
 // step as overflowed (so it is skipped and nothing changes), stops issuing
 // copies, waits (again bounded) for the copies it still has in flight, and
-// returns.
+// finishes.  When the launch ends the step, the CTA that finishes last
+// commits or skips it.
 #pragma once
 
 #include "kernels.cuh"
@@ -56,6 +57,8 @@ struct StagedParams {
     const float *w0, *w1, *m0, *m1, *v0, *v1;
     float *wo0, *wo1, *mo0, *mo1, *vo0, *vo1;
     uint16_t *par0, *par1;
+    int32_t end_step;  // the CTA that finishes last ends the step (a8)
+    FinCfg fin;
 };
 
 __device__ __forceinline__ bool stage_ready(uint32_t bar, uint32_t parity)
@@ -220,9 +223,11 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
                         break;
             }
         }
-        return;
+    } else {
+        flag_nonfinite(bad, &p.state->found_inf);
     }
-    flag_nonfinite(bad, &p.state->found_inf);
+    if (p.end_step)
+        arrive_and_end_step(p.fin, p.state);
 }
 
 }  // namespace zs

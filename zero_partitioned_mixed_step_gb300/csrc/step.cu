@@ -49,6 +49,11 @@ __host__ __device__ constexpr bool second_pass(int m)
     return m == M_PASS2_RECOMPUTE || m == M_PASS2_STAGED || m == M_ACC_PASS2;
 }
 __host__ __device__ constexpr bool reduces_only(int m) { return m == M_RS || m == M_RS_ACC; }
+// Modes that can be the last kernel of a step (and then end it themselves).
+__host__ __device__ constexpr bool ends_step(int m)
+{
+    return m == M_FUSED || m == M_ACC_FUSED || second_pass(m);
+}
 
 template <int MAXW>
 struct StepParams {
@@ -72,17 +77,15 @@ struct StepParams {
     // 128-byte aligned), so they are never written back to DRAM.
     int64_t keep_from;
     int32_t discard;
+    // The step's last kernel: the CTA that finishes last ends the step (a8).
+    int32_t end_step;
+    FinCfg fin;
 };
 
-// HOST_STATE: master, m and v live in pinned host memory (offload).  Its
-// instances are held to 5 resident CTAs per SM (at most 51 registers): host
-// accesses take microseconds, so more warps in flight pay.  Timed on the
-// 1.5B, 16-rank offloaded step: 156 ms at 5 CTAs/SM against 174 ms at the
-// natural 3 (and 225 ms at 4, 196 ms at 6: the register caps also reorder the
-// loads).
-template <int DT, int W, int MAXW, int MODE, bool ALL, bool HOST_STATE = false>
-__global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
-    step_kernel(const __grid_constant__ StepParams<MAXW> p)
+// The body of the streaming kernels (the __global__ wrappers below differ
+// only in their launch bounds).
+template <int DT, int W, int MAXW, int MODE, bool ALL, bool HOST_STATE>
+__device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
 {
     __shared__ Scalars sh;
     __shared__ int sh_cur;
@@ -114,16 +117,17 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
         __syncthreads();
         s = sh;
         cur = sh_cur;
-        if constexpr (second_pass(MODE)) {
-            if (s.skip) {  // the whole step is skipped: write nothing
-                if constexpr (MODE == M_PASS2_STAGED) {
-                    if (p.discard)  // the kept stage lines are not needed either
-                        for (int64_t u = p.keep_from +
-                                         4 * ((int64_t)blockIdx.x * kThreads + threadIdx.x);
-                             u + 4 <= vw.units; u += 4 * stride)
-                            discard_l2_line(p.stage + u * kUnit);
-                }
-                return;
+    }
+    bool work = true;
+    if constexpr (second_pass(MODE)) {
+        if (s.skip) {  // the whole step is skipped: write nothing
+            work = false;
+            if constexpr (MODE == M_PASS2_STAGED) {
+                if (p.discard)  // the kept stage lines are not needed either
+                    for (int64_t u = p.keep_from +
+                                     4 * ((int64_t)blockIdx.x * kThreads + threadIdx.x);
+                         u + 4 <= vw.units; u += 4 * stride)
+                        discard_l2_line(p.stage + u * kUnit);
             }
         }
     }
@@ -231,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
     };
 
     const int64_t base = (int64_t)blockIdx.x * kThreads;
-    if constexpr (second_pass(MODE)) {
+    if (!work) {
+    } else if constexpr (second_pass(MODE)) {
         // Backwards over the grid-stride sequence: the units the first pass
         // reached last come first, while their lines can still be in L2.
         if (base < vw.units) {
@@ -261,6 +266,33 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
         if (threadIdx.x == 0)
             p.partials[blockIdx.x] = tot;
     }
+    if constexpr (ends_step(MODE)) {
+        if (p.end_step)
+            arrive_and_end_step(p.fin, p.state);
+    }
+}
+
+// Device-resident state: the launch bound names only the block size, and
+// ptxas keeps these instances at 46-80 registers (3 CTAs of 256 threads per
+// SM).  A minimum of one CTA per SM in the bound lets it spend up to 255
+// (252 for the 64-rank shard), which costs two thirds of the warps.
+template <int DT, int W, int MAXW, int MODE, bool ALL>
+__global__ void __launch_bounds__(kThreads)
+    step_kernel(const __grid_constant__ StepParams<MAXW> p)
+{
+    step_body<DT, W, MAXW, MODE, ALL, false>(p);
+}
+
+// Master, m and v in pinned host memory (offload): held to 5 resident CTAs
+// per SM (at most 51 registers).  Host accesses take microseconds, so more
+// warps in flight pay: timed on the 1.5B, 16-rank offloaded step, 156 ms at 5
+// CTAs/SM against 174 ms at the natural 3 (225 ms at 4, 196 ms at 6: the
+// register caps also reorder the loads).
+template <int DT, int W, int MAXW, int MODE, bool ALL>
+__global__ void __launch_bounds__(kThreads, 5)
+    step_kernel_host_state(const __grid_constant__ StepParams<MAXW> p)
+{
+    step_body<DT, W, MAXW, MODE, ALL, true>(p);
 }
 
 // ------------------------------------------------------------------ launch
@@ -268,8 +300,13 @@ __global__ void __launch_bounds__(kThreads, HOST_STATE ? 5 : 1)
 template <int DT, int W, int MAXW, int MODE, bool HOST_STATE = false>
 int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
 {
-    auto kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true, HOST_STATE>
-                                 : step_kernel<DT, W, MAXW, MODE, false, HOST_STATE>;
+    void (*kern)(StepParams<MAXW>);
+    if constexpr (HOST_STATE)
+        kern = p.view.all_ranks ? step_kernel_host_state<DT, W, MAXW, MODE, true>
+                                : step_kernel_host_state<DT, W, MAXW, MODE, false>;
+    else
+        kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true>
+                                : step_kernel<DT, W, MAXW, MODE, false>;
     const int target = target_ctas(reinterpret_cast<const void *>(kern));
     const int64_t want = (p.view.units + kThreads - 1) / kThreads;
     const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
@@ -357,6 +394,7 @@ struct PassArgs {
     int n_partials = 0;       // second passes: CTAs of the first pass
     int64_t keep_from = INT64_MAX;  // clipped steps: see StepParams
     bool discard = false;
+    bool end_step = false;    // the launch is the step's last: it ends the step
 };
 
 // The one-pass step with the optimizer state in pinned host memory: one
@@ -417,6 +455,9 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
     p.add = a.add;
     p.keep_from = a.keep_from < v.units ? a.keep_from : v.units;
     p.discard = a.discard && p.keep_from < v.units ? 1 : 0;
+    p.end_step = a.end_step ? 1 : 0;
+    if (a.cfg)
+        p.fin = fin_cfg(*a.cfg);
     if (a.host_state)
         return dispatch_host_state<MAXW>(p, a.dtype, stream, gx);
     return dispatch<MAXW>(p, a.dtype, mode, stream, gx);
@@ -578,6 +619,8 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
     p.v1 = p.vo1 = a.v[1];
     p.par0 = static_cast<uint16_t *>(a.params[0]);
     p.par1 = static_cast<uint16_t *>(a.params[1]);
+    p.end_step = a.end_step ? 1 : 0;
+    p.fin = fin_cfg(c);
     return is_bf16(a.dtype) ? launch_staged_w<ZERO_BF16, kStagedWorld>(p, stream)
                             : launch_staged_w<ZERO_F16, kStagedWorld>(p, stream);
 }
@@ -590,38 +633,39 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
 #endif
 constexpr int64_t kKeepBytes = (int64_t)ZS_KEEP_MB << 20;
 
-// One step (one or two passes, then the finalize unless commit is false) in
-// the given modes.  A clipped step's second pass reduces the first pass's
-// per-CTA sums of squares itself (there is no separate norm kernel).
+// One step (one or two passes) in the given modes.  With commit the step's
+// last launch also ends the step (a8: its last CTA commits or skips); an empty
+// vector runs no pass and ends the step with the one-thread kernel.  A clipped
+// step's second pass reduces the first pass's per-CTA sums of squares itself
+// (there is no separate norm kernel).
 int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream,
              bool commit = true)
 {
     int rc, gx = 1;
     const zero_layout &L = *a.lay;
-    if (L.padded_numel > 0) {
-        if (!clip) {
-            rc = one_pass == M_FUSED ? launch_staged(a, stream) : 1;
-            if (rc == 1)
-                rc = run(a, one_pass, stream, &gx);
-            if (rc)
-                return rc;
-        } else {
-            const int64_t units = (a.rank < 0 ? L.padded_numel : L.owned_numel) / kUnit;
-            const bool regrads = pass1 == M_PASS1 && !a.stage;  // pass 2 reduces again
-            const int64_t kept = kKeepBytes / (regrads ? 2 * kUnit * (int64_t)L.world : 4 * kUnit);
-            int64_t from = units > kept ? units - kept : 0;
-            from = (from + 3) / 4 * 4;
-            a.keep_from = from < units ? from : units;
-            a.discard = a.stage && pass2 == M_PASS2_STAGED &&
-                        (reinterpret_cast<uintptr_t>(a.stage) & 127u) == 0;
-            if ((rc = run(a, pass1, stream, &gx)))
-                return rc;
-            a.n_partials = gx;
-            if ((rc = run(a, pass2, stream, &gx)))
-                return rc;
-        }
+    if (L.padded_numel == 0)
+        return commit ? launch_finalize(a.cfg, a.state, 1, stream) : ZERO_OK;
+    if (!clip) {
+        a.end_step = commit;
+        rc = one_pass == M_FUSED ? launch_staged(a, stream) : 1;
+        if (rc == 1)
+            rc = run(a, one_pass, stream, &gx);
+        return rc;
     }
-    return commit ? launch_finalize(a.cfg, a.state, 1, stream) : ZERO_OK;
+    const int64_t units = (a.rank < 0 ? L.padded_numel : L.owned_numel) / kUnit;
+    const bool regrads = pass1 == M_PASS1 && !a.stage;  // pass 2 reduces again
+    const int64_t kept = kKeepBytes / (regrads ? 2 * kUnit * (int64_t)L.world : 4 * kUnit);
+    int64_t from = units > kept ? units - kept : 0;
+    from = (from + 3) / 4 * 4;
+    a.keep_from = from < units ? from : units;
+    a.discard = a.stage && pass2 == M_PASS2_STAGED &&
+                (reinterpret_cast<uintptr_t>(a.stage) & 127u) == 0;
+    a.end_step = false;
+    if ((rc = run(a, pass1, stream, &gx)))
+        return rc;
+    a.n_partials = gx;
+    a.end_step = commit;
+    return run(a, pass2, stream, &gx);
 }
 
 }  // namespace zs
