@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from synth.workloads import CFG2, CFG3, CFG4, CFG5, PERBUCKET_CFG3
+from synth.workloads import CFG2, CFG3, CFG4, CFG5, OFFLOAD_CFG3, PERBUCKET_CFG3
 import zero_partitioned_mixed_step_gb300 as zs
 from zs_harness import (INF_BITS, SUMSQ_RTOL, assert_close, assert_half_close, half_bits,
                         lib_cfg, oracle_cfg)
@@ -47,15 +47,23 @@ class GpuGroup:
         rank = -1 if wl.rank is None else wl.rank
         self.z = zs.ZeroStep(wl.numels, wl.world, wl.dtype, lib_cfg(wl), loss_scale=wl.loss_scale,
                              rank=rank, bucket_numel=wl.bucket, align_elems=wl.align,
-                             grads_are_slices=wl.grads_are_slices, stage_grad=stage)
+                             grads_are_slices=wl.grads_are_slices, stage_grad=stage,
+                             offload_state=wl.offload_state)
         self.gaps = synth.gaps(self.lay.offsets, wl.numels, self.lay.padded)
         self.segs = ([(0, self.lay.padded)] if wl.rank is None else
                      list(self.lay.segments[wl.rank]))
-        self._fill_by_flat(self.z.master[0],
+        # offloaded state: generate the weights on the device, then copy them
+        # into the page-locked host buffer
+        master0 = (self.z.master[0] if self.z.master[0].is_cuda else
+                   torch.empty(self.z.master[0].numel(), dtype=torch.float32, device="cuda"))
+        self._fill_by_flat(master0,
                            lambda o, fs: synth.gpu_fill_f32(wl.master_key(), fs, o,
                                                             wl.master_sigma))
         if wl.rank is None:
-            synth.gpu_round_half(self.z.master[0], self.z.params[0], wl.dtype)
+            synth.gpu_round_half(master0, self.z.params[0], wl.dtype)
+        if master0 is not self.z.master[0]:
+            self.z.master[0].copy_(master0)
+            del master0
         hdt = zs.torch_dtype(wl.dtype)
         n = self.lay.owned if wl.grads_are_slices else self.lay.padded
         self.grads = [torch.empty(n, dtype=hdt, device="cuda") for _ in range(wl.world)]
@@ -258,6 +266,14 @@ def test_fullsize_1p5B_nd16_per_bucket():
     """The 1.5B, 16-rank workload in 60 buckets of 25,000,064 elements, run
     as one launch per bucket on two streams and one commit; +Inf in step 2."""
     st = run_windowed(PERBUCKET_CFG3.replace(inject_every=2), steps=3)
+    assert st.skipped == 1 and st.t == 2
+
+
+def test_fullsize_1p5B_nd16_offloaded_state():
+    """The 1.5B, 16-rank step with master, m and v in page-locked host
+    memory (6 GB per buffer: huge-page blocks registered with the driver),
+    read and written by the kernel over the host link; +Inf in step 2."""
+    st = run_windowed(OFFLOAD_CFG3.replace(inject_every=2), steps=3)
     assert st.skipped == 1 and st.t == 2
 
 

@@ -72,6 +72,29 @@ def test_clip_staged_and_recomputed_agree(stage):
         ls.check()
 
 
+@pytest.mark.parametrize("offset_floats", [0, 8], ids=["stage-128B-aligned", "stage-32B-off"])
+@pytest.mark.parametrize("numels,world", [((8 * 1001 + 3,), 1), ((3 * 8 * 777 + 5,), 3)],
+                         ids=["one-rank", "three-ranks"])
+def test_clip_stage_alignment_and_ragged_units(numels, world, offset_floats):
+    """The clipped step's second pass drops the kept stage lines from L2 only
+    when the stage is 128-byte aligned, and only whole 128-byte lines inside
+    the buffer.  A stage 32 bytes off a 128-byte boundary (no line is
+    dropped) and vectors whose count of 8-element units is not a multiple of
+    4 (8-element tensor alignment: the last line is partial) give the
+    oracle's results all the same, step after step."""
+    wl = CFG2.replace(numels=numels, world=world, align=8, max_grad_norm=0.01, steps=3)
+    ls = Lockstep(wl, stage=True)
+    n = ls.z.g_stage.numel()
+    assert (n // 8) % 4 != 0  # a partial last line
+    buf = torch.empty(n + 32, dtype=torch.float32, device="cuda")
+    ls.z.g_stage = buf[offset_floats:offset_floats + n]
+    assert (ls.z.g_stage.data_ptr() % 128 == 0) == (offset_floats == 0)
+    for _ in range(wl.steps):
+        ls.step()
+        st = ls.check()
+        assert st.clip_coef < 1.0  # the clip is active
+
+
 EDGE = {
     "one-rank": CFG1.replace(numels=(70_001,), world=1, steps=2, inject_at=()),
     "three-ranks-generic": CFG1.replace(numels=(100_003, 17), world=3, steps=3,
