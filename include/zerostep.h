@@ -235,7 +235,12 @@ ZERO_API int zero_host_free(void *p);
 /*
  * Step (a2): reduce-scatter sum, g[j] = sum over q = 0 .. world-1 of
  * float(grads[q][.]) in ascending q, fp32, not unscaled.
- *  grads: HOST array of `world` DEVICE pointers, one gradient buffer per rank.
+ *  grads: HOST array of `world` pointers, one gradient buffer per rank: device
+ *    memory, or page-locked host memory mapped into the device's address
+ *    space (zero_host_alloc, cudaHostAlloc, cudaHostRegister), which the
+ *    kernels then load directly over the host link (no copy into device
+ *    memory; on GB300 the loads of 16 such buffers ran at 210 GB/s, the
+ *    link's rate, where copy engines gave 94-155 GB/s).
  *  grads_are_slices: 0 = each buffer is the full padded flat vector;
  *    1 = each buffer holds only the elements `rank` owns, in order (needs rank >= 0).
  *  rank = -1: every partition; g_out (device, padded_numel floats) is in flat

@@ -504,20 +504,60 @@ def test_host_blocks_round_trip():
     del h, back  # blocks are released with their last tensor
 
 
-def test_step_from_host_matches_device_step():
-    """step_from_host (gradients copied in from page-locked host blocks, the
-    step, the state read back) gives the same bits as the step on gradients
-    made on the device."""
-    wl = CFG1.replace(numels=(300_001,), world=4, steps=2, inject_at=())
-    a, b = Lockstep(wl), Lockstep(wl)
+FROM_HOST = {
+    # 16 ranks, every rank: on the device this is the shared-memory staged kernel
+    "nd16-all-ranks": CFG1.replace(numels=(200_001,), world=16, steps=2, inject_at=((2, 9, 77),)),
+    "nd4-fp16": CFG1.replace(numels=(300_001,), world=4, steps=2, inject_at=()),
+    "nd8-bf16-clip-staged": CFG2.replace(numels=_small_gpt2(), steps=2),
+    "nd4-rank2-slices": CFG4.replace(numels=(4 * 40_000 + 8,), world=4, rank=2, steps=2,
+                                     inject_at=()),
+    "nd8-bf16-halfreduce": CFG1.replace(numels=(100_000,), world=8, dtype=synth.BF16,
+                                        half_reduce=True, steps=2, inject_at=()),
+}
+
+
+@pytest.mark.parametrize("copy", [False, True], ids=["loaded-from-host", "copied-in"])
+@pytest.mark.parametrize("name", list(FROM_HOST))
+def test_step_from_host_matches_device_step(name, copy):
+    """step_from_host with each rank's gradient in a page-locked host block,
+    either loaded by the step's kernels straight over the host link or
+    copied into device buffers first, gives the same bits as the step on
+    gradients in device memory (which the oracle checks), including a
+    skipped step."""
+    wl = FROM_HOST[name]
+    a = Lockstep(wl, stage=True) if wl.max_grad_norm > 0 else Lockstep(wl)
+    b = Lockstep(wl, stage=True) if wl.max_grad_norm > 0 else Lockstep(wl)
     for s in range(1, wl.steps + 1):
         grads = gen_grads(wl, a.lay, s, a.st.loss_scale)
         a.step(grads)
         src = [to_dev_half(g, wl.dtype) for g in grads]
         host = [zs.host_empty(g.numel(), g.dtype).copy_(g.cpu()) for g in src]
-        st = b.z.step_from_host(host, [torch.empty_like(g) for g in src])
-        assert st.error == 0 and st.t == s
+        dev = [torch.empty_like(g) for g in src] if copy else None
+        st = b.z.step_from_host(host, dev)
+        assert st.error == 0 and st.t + st.skipped == s
     a.check()
+    for x, y in zip(a.z.current(), b.z.current()):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    assert a.z.read_state().t == b.z.read_state().t
+
+
+def test_accumulation_from_host_matches_device():
+    """Micro-steps whose gradients the accumulation kernel loads straight
+    from page-locked host blocks give the same bits as from device buffers."""
+    wl = CFG1.replace(numels=(100_003,), world=8, steps=1, inject_at=())
+    a, b = Lockstep(wl), Lockstep(wl)
+    micro = 3
+    src = [[to_dev_half(g, wl.dtype) for g in gen_grads(wl, a.lay, k + 1, wl.loss_scale)]
+           for k in range(micro)]
+    for k in range(micro):
+        a.z.accumulate(src[k], k > 0)
+        host = [zs.host_empty(g.numel(), g.dtype).copy_(g.cpu()) for g in src[k]]
+        b.z.accumulate(host, k > 0)
+        torch.cuda.synchronize()
+    a.z.step_accumulated()
+    b.z.step_accumulated()
+    torch.cuda.synchronize()
+    assert torch.equal(a.z.acc.view(torch.int32), b.z.acc.view(torch.int32))
     for x, y in zip(a.z.current(), b.z.current()):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
 

@@ -70,6 +70,12 @@ def _state_array(tensors: Sequence[torch.Tensor]):
     return (ctypes.c_void_p * len(tensors))(*[_state_ptr(t) for t in tensors])
 
 
+def _grad_array(tensors: Sequence[torch.Tensor]):
+    """Gradient buffers: CUDA tensors, or pinned host tensors that the
+    kernels load directly over the host link."""
+    return _state_array(tensors)
+
+
 def _stream(stream) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -165,7 +171,7 @@ def zero_reduce_scatter_sum(grads: Sequence[torch.Tensor], layout: Layout, g_out
                             rank: int = -1, grads_are_slices: bool = False, stream=None,
                             half_reduce: bool = False) -> None:
     check("zero_reduce_scatter_sum",
-          lib().zero_reduce_scatter_sum(_ptr_array(grads), int(grads_are_slices),
+          lib().zero_reduce_scatter_sum(_grad_array(grads), int(grads_are_slices),
                                         _grad_code(grads, half_reduce), ctypes.byref(layout),
                                         rank, _dev_ptr(g_out), _stream(stream)))
 
@@ -216,7 +222,7 @@ def zero_step_fused(grads: Sequence[torch.Tensor], layout: Layout,
     ping-pong slots (the same tensor twice for an in-place clipped step);
     master, m and v may be pinned host tensors (offloaded state)."""
     check("zero_step_fused",
-          lib().zero_step_fused(_ptr_array(grads), int(grads_are_slices),
+          lib().zero_step_fused(_grad_array(grads), int(grads_are_slices),
                                 _grad_code(grads, half_reduce),
                                 ctypes.byref(layout), rank, _state_array(master), _state_array(m),
                                 _state_array(v), _ptr_array(params), _dev_ptr(g_stage),
@@ -234,7 +240,7 @@ def zero_step_fused_buckets(grads: Sequence[torch.Tensor], layout: Layout, first
     first_bucket + n_buckets), without the commit; zero_step_finalize(cfg,
     state, flip_slot=True) commits once every bucket has been processed."""
     check("zero_step_fused_buckets",
-          lib().zero_step_fused_buckets(_ptr_array(grads), int(grads_are_slices),
+          lib().zero_step_fused_buckets(_grad_array(grads), int(grads_are_slices),
                                         _grad_code(grads, half_reduce), ctypes.byref(layout),
                                         rank, first_bucket, n_buckets, _state_array(master),
                                         _state_array(m), _state_array(v), _ptr_array(params),
@@ -248,7 +254,7 @@ def zero_reduce_scatter_accumulate(grads: Sequence[torch.Tensor], layout: Layout
     """One micro-step of gradient accumulation: acc = (acc if add else 0) +
     the reduce-scatter sum of the ranks' half gradients."""
     check("zero_reduce_scatter_accumulate",
-          lib().zero_reduce_scatter_accumulate(_ptr_array(grads), int(grads_are_slices),
+          lib().zero_reduce_scatter_accumulate(_grad_array(grads), int(grads_are_slices),
                                                _grad_code(grads, half_reduce),
                                                ctypes.byref(layout), rank,
                                                _dev_ptr(acc), int(add), _stream(stream)))
@@ -368,25 +374,31 @@ class ZeroStep:
                                     stream)
 
     def step_from_host(self, host_grads: Sequence[torch.Tensor],
-                       device_grads: Sequence[torch.Tensor], stream=None,
+                       device_grads: Optional[Sequence[torch.Tensor]] = None, stream=None,
                        micro_steps: int = 1) -> StepState:
-        """End to end: copy each rank's gradient from (pinned) host memory, run
-        the step and read the step state back to the host.  With
-        micro_steps > 1 the copy is repeated for every micro-step (the same
-        host buffers stand for each) and accumulated before the step."""
+        """End to end from each rank's gradient in page-locked host memory:
+        run the step and read the step state back to the host.  Without
+        device_grads the step's kernels load the gradients straight from the
+        host buffers over the host link; with device_grads each gradient is
+        first copied into its device buffer by the copy engines.  With
+        micro_steps > 1 the same host buffers stand for every micro-step, each
+        reduced into the fp32 accumulator before the step."""
         s = stream if stream is not None else torch.cuda.current_stream()
         if getattr(self, "_state_host", None) is None:
             self._state_host = host_empty(64, torch.uint8)
         with torch.cuda.stream(s):
             for k in range(micro_steps):
-                for h, d in zip(host_grads, device_grads):
-                    d.copy_(h, non_blocking=True)
+                grads = host_grads
+                if device_grads is not None:
+                    for h, d in zip(host_grads, device_grads):
+                        d.copy_(h, non_blocking=True)
+                    grads = device_grads
                 if micro_steps > 1:
-                    self.accumulate(device_grads, k > 0, s)
+                    self.accumulate(grads, k > 0, s)
             if micro_steps > 1:
                 self.step_accumulated(s)
             else:
-                self.step(device_grads, s)
+                self.step(grads, s)
             self._state_host.copy_(self.state, non_blocking=True)
         s.synchronize()
         return StepState.from_buffer_copy(bytes(self._state_host.numpy().tobytes()))

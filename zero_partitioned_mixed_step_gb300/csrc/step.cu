@@ -602,6 +602,11 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
     if (a.rank >= 0 || a.host_state || half_reduce(a.dtype) || L.world != kStagedWorld ||
         stages < 2 || L.padded_numel <= 0)
         return 1;
+    // The bulk copies serve gradients in device memory; gradients in
+    // page-locked host memory are loaded by the register kernel.
+    for (int q = 0; q < L.world; ++q)
+        if (residence(a.grads[q]) != 0)
+            return 1;
     StagedParams p{};
     for (int q = 0; q < L.world; ++q)
         p.g[q] = static_cast<const uint16_t *>(a.grads[q]);
