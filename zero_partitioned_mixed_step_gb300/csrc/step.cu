@@ -235,11 +235,10 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     };
 
     const int64_t base = (int64_t)blockIdx.x * kThreads;
-    if (!work) {
-    } else if constexpr (second_pass(MODE)) {
+    if constexpr (second_pass(MODE)) {
         // Backwards over the grid-stride sequence: the units the first pass
         // reached last come first, while their lines can still be in L2.
-        if (base < vw.units) {
+        if (work && base < vw.units) {
             for (int64_t k = (vw.units - 1 - base) / stride; k >= 0; --k) {
                 const int64_t first = base + k * stride;  // the CTA's first unit this round
                 const int64_t u = first + threadIdx.x;
