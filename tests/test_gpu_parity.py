@@ -6,6 +6,8 @@ CTAs, several ranks and ragged tails; every workload's structure (tensor
 list, alignment, buckets, rank view, dtype, loss scaling, clipping,
 overflow injection) is exercised.  Full-size workloads are in
 test_gpu_fullsize.py."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -482,6 +484,40 @@ def test_staged_path_matches_register_path(world, dtype):
         assert torch.equal(fm[idx].view(torch.int32), m.view(torch.int32))
         assert torch.equal(fv[idx].view(torch.int32), v.view(torch.int32))
         assert np.array_equal(pb[idx.cpu().numpy()], half_bits(p)[idx.cpu().numpy()])
+
+
+def test_staged_wait_that_runs_out_skips_the_step_and_reports():
+    """Every mbarrier wait of the shared-memory staged kernel is bounded.
+    With ZERO_TEST_STAGED_WAIT_LIMIT set, each stage is announced 16 bytes
+    more than its copies bring, so every CTA's first wait runs out after 1000
+    polls: the kernel records state.error, skips the step (every buffer's
+    current slot unchanged bit for bit, the dynamic loss scale backed off),
+    retires the extra bytes, waits for its own copies and finishes.  With the
+    error cleared, the next step commits in lockstep with the oracle."""
+    wl = CFG1.replace(numels=(200_001,), world=16, steps=3, inject_at=(), dynamic_scale=True)
+    ls = Lockstep(wl)
+    ls.step()
+    ls.check()
+    before = [t.clone() for t in ls.z.current()]
+    grads = gen_grads(wl, ls.lay, 2, ls.st.loss_scale)
+    os.environ["ZERO_TEST_STAGED_WAIT_LIMIT"] = "1000"
+    try:
+        ls.z.step([to_dev_half(g, wl.dtype) for g in grads])
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["ZERO_TEST_STAGED_WAIT_LIMIT"]
+    st = ls.z.read_state()
+    assert (st.error, st.overflow, st.skipped, st.t, st.found_inf) == (1, 1, 1, 1, 0)
+    assert st.loss_scale == wl.loss_scale / 2
+    for a, b in zip(before, ls.z.current()):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    oracle.skip(ls.ocfg, ls.st)  # the oracle's view of the same step
+    ls.steps += 1
+    off = zs.StepState.error.offset
+    ls.z.state[off:off + 4].zero_()  # the caller has handled the error
+    ls.step()
+    st = ls.check()
+    assert st.t == 2 and st.skipped == 1
 
 
 # ----------------------------------------------------------------- page-locked host blocks

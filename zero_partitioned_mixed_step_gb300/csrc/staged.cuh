@@ -22,7 +22,13 @@
 // step as overflowed (so it is skipped and nothing changes), stops issuing
 // copies, waits (again bounded) for the copies it still has in flight, and
 // finishes.  When the launch ends the step, the CTA that finishes last
-// commits or skips it.
+// commits or skips it.  A test exercises that path on the GPU: with the
+// environment variable ZERO_TEST_STAGED_WAIT_LIMIT=n the launch polls a stage
+// at most n times and announces 16 bytes more to each stage's mbarrier than
+// its copies bring, so the first wait runs out.  The drain then retires the
+// 16 bytes itself (mbarrier.complete_tx), so its wait ends exactly when the
+// stage's real copies have landed: no copy is in flight when the CTA
+// finishes.
 #pragma once
 
 #include "kernels.cuh"
@@ -59,6 +65,8 @@ struct StagedParams {
     uint16_t *par0, *par1;
     int32_t end_step;  // the CTA that finishes last ends the step (a8)
     FinCfg fin;
+    long long spin_limit;  // polls of a stage's mbarrier before giving up
+    uint32_t tx_extra;     // 0; > 0 only when a test makes every wait run out
 };
 
 __device__ __forceinline__ bool stage_ready(uint32_t bar, uint32_t parity)
@@ -134,7 +142,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
         // the threads' earlier reads of this stage come before the copies' writes
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"(len * 2u * (uint32_t)world + 3u * len * 4u)
+                     "r"(len * 2u * (uint32_t)world + 3u * len * 4u + p.tx_extra)
                      : "memory");
 #pragma unroll
         for (int q = 0; q < W; ++q)
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
         const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&full[st]);
         const uint32_t parity = (uint32_t)((k / nst) & 1);
         bool ready = false;
-        for (long long it = 0; it < kStageSpinLimit; ++it)
+        for (long long it = 0; it < p.spin_limit; ++it)
             if (stage_ready(bar, parity)) {
                 ready = true;
                 break;
@@ -218,6 +226,10 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
                 if (t >= tiles)
                     break;
                 const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&full[kk % nst]);
+                if (p.tx_extra)  // the announced extra bytes never come: retire them
+                    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar),
+                                 "r"(p.tx_extra)
+                                 : "memory");
                 for (long long it = 0; it < kStageSpinLimit; ++it)
                     if (stage_ready(bar, (uint32_t)((kk / nst) & 1)))
                         break;

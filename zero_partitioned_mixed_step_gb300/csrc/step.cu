@@ -20,6 +20,8 @@
 //   ACC_*      the step with the gradient read from an fp32 accumulator (the
 //              sum of micro-steps' reduced, still scaled gradients) instead of
 //              the N_d half buffers: FUSED, PASS1 and PASS2 as above.
+#include <cstdlib>
+
 #include "kernels.cuh"
 #include "staged.cuh"
 
@@ -625,6 +627,15 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
     p.par1 = static_cast<uint16_t *>(a.params[1]);
     p.end_step = a.end_step ? 1 : 0;
     p.fin = fin_cfg(c);
+    p.spin_limit = kStageSpinLimit;
+    p.tx_extra = 0;
+    if (const char *t = std::getenv("ZERO_TEST_STAGED_WAIT_LIMIT")) {  // tests only
+        const long long n = std::atoll(t);
+        if (n > 0) {
+            p.spin_limit = n;
+            p.tx_extra = 16;
+        }
+    }
     return is_bf16(a.dtype) ? launch_staged_w<ZERO_BF16, kStagedWorld>(p, stream)
                             : launch_staged_w<ZERO_F16, kStagedWorld>(p, stream);
 }
