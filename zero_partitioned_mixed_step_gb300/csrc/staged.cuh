@@ -1,12 +1,14 @@
-// The one-pass fused step (a2)-(a7) with its inputs staged through shared
-// memory by the Tensor Memory Accelerator's bulk copies.
+// The one-pass fused step (a2)-(a7), and (a8) when the launch ends the step,
+// with its inputs staged through shared memory by the Tensor Memory
+// Accelerator's bulk copies.
 //
 // Used for every-rank launches over the flat vector with the reduction in
-// fp32, device-resident state and N_d = 16 (a compile-time constant, so the
-// shared-memory reads and the copies unroll).  Measured on GB300 against the
-// register kernel on the same buffers, it is 0.7 % faster at N_d = 16 and
-// slower at N_d = 8 (1 %) and N_d = 4 (8 %), where the fp32 state dominates
-// the traffic; with 256 threads and one CTA per SM it lost at every N_d.
+// fp32, state and gradients in device memory and N_d = 16 (a compile-time
+// constant, so the shared-memory reads and the copies unroll).  Measured on
+// GB300 against the register kernel on the same buffers, it is 0.9 % faster
+// at N_d = 16 with fp16 gradients (1.8 % with bf16) and slower at N_d = 8
+// (1 %) and N_d = 4 (8 %), where the fp32 state dominates the traffic; with
+// 256 threads and one CTA per SM it lost at every N_d.
 // Each CTA (128 threads, two per SM) walks tiles of 1024 elements with a grid
 // stride.  For a tile, one thread issues N_d + 3 one-dimensional bulk copies
 // (cp.async.bulk, marked evict-first in L2): each rank's 2 KB gradient slice
