@@ -56,8 +56,19 @@ def algorithmic_bytes_per_elem(world: int, clip: bool, staged: bool, micro: int 
 STEP_KERNEL_SOURCES = ("step.cu", "kernels.cuh", "internal.h", "staged.cuh")
 
 
+def _code_only(data: bytes) -> bytes:
+    """C/C++ source without its comments and with runs of whitespace collapsed,
+    so that an edit to comments alone keeps the hash."""
+    import re
+    text = data.decode("utf-8")
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
+
+
 def kernel_source_hash(read=None) -> str:
-    """Hash of the sources the fused step kernel is compiled from."""
+    """Hash of the code (comments stripped) of the sources the fused step
+    kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "zero_partitioned_mixed_step_gb300", "csrc")
     for name in STEP_KERNEL_SOURCES:
@@ -66,7 +77,7 @@ def kernel_source_hash(read=None) -> str:
                 data = f.read()
         else:
             data = read(name)
-        h.update(name.encode() + data)
+        h.update(name.encode() + _code_only(data))
     return h.hexdigest()[:16]
 
 

@@ -382,8 +382,8 @@ ZERO_API int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state
  *    master that keeps the reduced gradient between the passes instead of
  *    reducing it twice (2 * N_d bytes read per element are replaced by 8).
  *    It is scratch: its contents after the call are undefined (the second
- *    pass drops the lines it no longer needs from L2 without writing them
- *    back).
+ *    pass drops the lines it no longer needs from L2 without writing back
+ *    any that are still dirty).
  *  state_dev: device step state.  ws: device workspace of ws_bytes >=
  *    zero_workspace_bytes(layout->world).
  * Offload: master, m and v (all six slots) may instead be

@@ -76,7 +76,7 @@ struct StepParams {
     // units backwards, so it starts on what is still in L2.  keep_from is a
     // multiple of 4 (= units when nothing is kept).  discard: the second pass
     // drops the stage's kept lines from L2 after reading them (the stage is
-    // 128-byte aligned), so they are never written back to DRAM.
+    // 128-byte aligned), so a line still dirty is not written back to DRAM.
     int64_t keep_from;
     int32_t discard;
     // The step's last kernel: the CTA that finishes last ends the step (a8).
