@@ -394,6 +394,10 @@ ZERO_API int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state
  *  ZeRO", "配置说明": offload_optimizer.device = cpu).  The residence is
  *  detected per call (cudaPointerGetAttributes); mixed residence, or
  *  offloaded state together with the clip, is ZERO_EINVAL.
+ * CUDA graphs: the call synchronises nothing and ends the step on the device,
+ *  so it can be captured on a stream and replayed (gradients refreshed in the
+ *  same buffers); do one step of the same kind outside any capture first,
+ *  which fills the library's per-kernel caches.
  * Pages: all of the above; the ping-pong slots are this library's way to
  * skip a step bit-exactly without a second pass over the gradients.
  */
