@@ -656,11 +656,13 @@ BUCKETED = {
 }
 
 
+@pytest.mark.parametrize("where", ["device", "host"], ids=["grads-on-device", "grads-in-host"])
 @pytest.mark.parametrize("name", list(BUCKETED))
-def test_bucket_ranges_then_commit_equal_fused_step(name):
+def test_bucket_ranges_then_commit_equal_fused_step(name, where):
     """The step run as ranges of buckets on two streams, then one commit,
     gives the fused step's bits (and both follow the oracle), including a
-    step skipped for an Inf that lies in a middle bucket."""
+    step skipped for an Inf that lies in a middle bucket; the ranges may
+    also load the gradients from page-locked host blocks."""
     base = BUCKETED[name]
     lay = oracle.layout(base.numels, base.world, base.align, base.bucket)
     nb = lay.num_buckets
@@ -678,6 +680,8 @@ def test_bucket_ranges_then_commit_equal_fused_step(name):
         grads = gen_grads(wl, ref.lay, s, ref.st.loss_scale)
         ref.step(grads)
         gd = [to_dev_half(g, wl.dtype) for g in grads]
+        if where == "host":
+            gd = [zs.host_empty(g.numel(), g.dtype).copy_(g.cpu()) for g in gd]
         ready = torch.cuda.Event()
         ready.record(s0)
         for st in side:
