@@ -1,5 +1,6 @@
-// The streaming kernels of the step and the entry points zero_step_fused and
-// zero_reduce_scatter_sum.
+// The streaming kernels of the step and the entry points zero_step_fused,
+// zero_step_fused_accumulated, zero_step_fused_buckets,
+// zero_reduce_scatter_sum and zero_reduce_scatter_accumulate.
 //
 // One kernel template covers the passes over the data.  Each thread handles
 // 8-element units (16-byte loads of each rank's half gradient, 32-byte loads
@@ -20,6 +21,10 @@
 //   ACC_*      the step with the gradient read from an fp32 accumulator (the
 //              sum of micro-steps' reduced, still scaled gradients) instead of
 //              the N_d half buffers: FUSED, PASS1 and PASS2 as above.
+// The last launch of a step (FUSED, a second pass, ACC_FUSED) also ends it:
+// the CTA that finishes last commits or skips the step (a8).  Gradient
+// buffers may be device memory or page-locked host memory, which these
+// kernels load over the host link.
 #include <cstdlib>
 
 #include "kernels.cuh"
