@@ -459,6 +459,19 @@ def window_step(grads: Sequence[np.ndarray], dtype: int, cfg: AdamCfg, st: State
     return f32_to_half(master, dtype)
 
 
+def finish_window_step(cfg: AdamCfg, st: State, flag: bool, total_sumsq: float) -> None:
+    """Step (a8) after every window of a step has gone through
+    ``window_step``: skip when the scan found NaN/Inf, else record the step's
+    sum of squares and clip coefficient (when clipping) and commit."""
+    if flag:
+        skip(cfg, st)
+        return
+    if cfg.max_grad_norm > 0:
+        st.sumsq = total_sumsq
+        st.coef = clip_coef(total_sumsq, cfg.max_grad_norm)
+    commit(cfg, st)
+
+
 # --------------------------------------------------------------------------
 # Gradient accumulation
 # --------------------------------------------------------------------------

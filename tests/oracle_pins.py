@@ -629,9 +629,132 @@ def pin_half_reduce():
     assert oracle.reduce_sum(big, oracle.F16, 0, 1)[0] == 120000.0
 
 
+
+# ----------------------------------------------------------------- the windowed path
+
+def _local_of(lay, r, flat):
+    local = 0
+    for fs, ln in lay.segments[r]:
+        if fs <= flat < fs + ln:
+            return local + flat - fs
+        local += ln
+    raise AssertionError("element not owned by the rank")
+
+
+def _windowed_problems():
+    """Small problems for the windowed path, each with its step-by-step
+    gradients: (name, layout, dtype, cfg, loss scale, rank, slices,
+    half_reduce, master, [grads of step 1, 2, 3])."""
+    out = []
+    # flat, 16 ranks, fp16 x 4096, dynamic scale; +Inf (rank 5) in step 2
+    lay, g1, master = _random_problem(16, (20_003,), oracle.F16, 31, scale=4096.0)
+    steps = [g1] + [_random_problem(16, (20_003,), oracle.F16, 31 + s, scale=4096.0)[1]
+                    for s in (1, 2)]
+    steps[1][5][12_345] = 0x7C00
+    out.append(("flat-nd16", lay, oracle.F16,
+                oracle.AdamCfg(dynamic_scale=True, max_grad_norm=1e30), 4096.0, None, False,
+                False, master, steps))
+    # buckets over 3 ranks, bf16, the clip active
+    args = (3, (5000, 77, 1200), oracle.BF16)
+    lay, g1, master = _random_problem(*args, 41, bucket=1536, scale=1.0)
+    steps = [g1] + [_random_problem(*args, 41 + s, bucket=1536, scale=1.0)[1] for s in (1, 2)]
+    out.append(("bucketed-clip", lay, oracle.BF16,
+                oracle.AdamCfg(weight_decay=0.01, max_grad_norm=0.01), 1.0, None, False, False,
+                master, steps))
+    # rank 2 of 4 over buckets, gradient buffers holding only rank 2's slices
+    args = (4, (4196, 300), oracle.F16)
+    lay, g1, master = _random_problem(*args, 51, bucket=4096)
+    steps = [g1] + [_random_problem(*args, 51 + s, bucket=4096)[1] for s in (1, 2)]
+    idx = np.concatenate([np.arange(fs, fs + ln) for fs, ln in lay.segments[2]])
+    steps = [[g[idx].copy() for g in gs] for gs in steps]
+    out.append(("rank-view-slices", lay, oracle.F16,
+                oracle.AdamCfg(weight_decay=0.01, max_grad_norm=1e30), 1024.0, 2, True, False,
+                master[idx].copy(), steps))
+    # reduction in bf16, 5 ranks, the clip active
+    args = (5, (3000,), oracle.BF16)
+    lay, g1, master = _random_problem(*args, 61, scale=1.0)
+    steps = [g1] + [_random_problem(*args, 61 + s, scale=1.0)[1] for s in (1, 2)]
+    out.append(("half-reduce", lay, oracle.BF16, oracle.AdamCfg(max_grad_norm=0.02), 1.0, None,
+                False, True, master, steps))
+    # per-rank sums whose binary64 total depends on the rank order: rank 0's
+    # sum of squares is 1, ranks 1-3 hold 2^-54 each; in rank order the total
+    # is 1, in reverse order 1 + 2^-52
+    lay = oracle.layout([256], 4)
+    one = torch.tensor([1.0, 2.0 ** -27]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    steps = []
+    for _ in range(3):
+        g = [np.zeros(lay.padded, np.uint16) for _ in range(4)]
+        g[0][0] = one[0]
+        for r in (1, 2, 3):
+            g[r][r * lay.owned + 3] = one[1]
+        steps.append(g)
+    out.append(("rank-order", lay, oracle.BF16, oracle.AdamCfg(max_grad_norm=1e30), 1.0, None,
+                False, False, np.zeros(lay.padded, np.float32), steps))
+    return out
+
+
+def pin_windowed_matches_step():
+    """The full-size parity tests check the GPU against the windowed path:
+    ``scan_scalars`` forms the step's overflow flag and sum of squares chunk
+    by chunk, and ``window_step`` steps any window of a rank's elements given
+    them (the update is element-wise once they are known: "DeepSpeed ZeRO",
+    ZeRO Stage 2, the derivation that a rank's optimizer-state shard needs
+    only its own gradient slice).  On small problems (16 ranks with an Inf in
+    a middle step, buckets with the clip, one rank's view with slice buffers,
+    the bf16 reduction, per-rank sums whose total depends on the rank order)
+    the flag and the sum of squares equal what ``step`` records, bit for bit,
+    and windows that tile every simulated element reproduce master, m, v and
+    the half parameters of ``step`` bit for bit over three steps."""
+    for (name, lay, dt, cfg, S, rank, slices, hr, master, steps) in _windowed_problems():
+        ranks = list(range(lay.world)) if rank is None else [rank]
+        n = master.size
+        ref = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32),
+               np.zeros(lay.padded, np.uint16)]
+        win = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32),
+               np.zeros(lay.padded, np.uint16)]
+        st_ref = oracle.State(loss_scale=S)
+        st_win = oracle.State(loss_scale=S)
+        lengths = (997, 64, 1500, 8, 333)
+        for s, grads in enumerate(steps, 1):
+            oracle.step(grads, dt, lay, cfg, st_ref, *ref, rank=rank, grads_are_slices=slices,
+                        half_reduce=hr)
+
+            def chunks(r, f0, cnt):
+                j = _local_of(lay, r, f0) if slices else f0
+                return [g[j:j + cnt] for g in grads]
+            flag, total = oracle.scan_scalars(chunks, dt, lay, oracle.f32(1.0 / st_win.loss_scale),
+                                              True, ranks=ranks, chunk=1000, half_reduce=hr)
+            assert flag == bool(st_ref.overflow), (name, s)
+            if not flag:
+                assert total == st_ref.sumsq, (name, s, total, st_ref.sumsq)
+            k = 0
+            for r in ranks:
+                local = 0
+                for fs, ln in lay.segments[r]:
+                    pos = 0
+                    while pos < ln:
+                        cnt = min(lengths[k % len(lengths)], ln - pos)
+                        k += 1
+                        si = fs + pos if rank is None else local + pos
+                        gi = local + pos if slices else fs + pos
+                        gw = [g[gi:gi + cnt].copy() for g in grads]
+                        h = oracle.window_step(gw, dt, cfg, st_win, flag, total,
+                                               win[0][si:si + cnt], win[1][si:si + cnt],
+                                               win[2][si:si + cnt], half_reduce=hr)
+                        if h is not None:
+                            win[3][fs + pos:fs + pos + cnt] = h
+                        pos += cnt
+                    local += ln
+            oracle.finish_window_step(cfg, st_win, flag, total)
+            for a, b in zip(ref, win):
+                assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), (name, s)
+            assert st_ref == st_win, (name, s, st_ref, st_win)
+
+
 ALL_PINS = [pin_memory_closed_forms, pin_decode_exhaustive, pin_encode_structured,
             pin_reduce_bruteforce, pin_reduce_order, pin_unscale_exact, pin_overflow_detect,
             pin_sumsq, pin_clip_coef, pin_adam_first_step, pin_adam_constant_grad,
             pin_adam_literal_form, pin_vs_torch, pin_partition_concat, pin_skip_invariance,
             pin_loss_scale_growth, pin_clip, pin_layout, pin_accumulate_exact,
-            pin_accumulate_order, pin_accumulated_step, pin_half_reduce]
+            pin_accumulate_order, pin_accumulated_step, pin_half_reduce,
+            pin_windowed_matches_step]

@@ -228,13 +228,7 @@ def run_windowed(wl, steps, stage=None):
             out = oracle.window_step(gw, wl.dtype, cfg, st, flag, sumsq, w, m, v)
             if out is not None:
                 h[:] = out
-        if flag:
-            oracle.skip(cfg, st)
-        else:
-            if cfg.max_grad_norm > 0:
-                st.sumsq = sumsq
-                st.coef = oracle.clip_coef(sumsq, cfg.max_grad_norm)
-            oracle.commit(cfg, st)
+        oracle.finish_window_step(cfg, st, flag, sumsq)
         torch.cuda.synchronize()
         zst = z.read_state()
         assert (zst.overflow, zst.t, zst.skipped, zst.loss_scale) == \

@@ -122,17 +122,55 @@ def _py_mutations():
                                  lay.flat_end, P * world, P, 1, P, P, segs)
         return lay
 
+    def scan_ranks_reversed(grad_chunks, dtype, lay, inv_scale, want_sumsq, openmp=False,
+                            ranks=None, chunk=1 << 24, half_reduce=False):
+        order = list(range(lay.world)) if ranks is None else list(ranks)
+        return orig_scan(grad_chunks, dtype, lay, inv_scale, want_sumsq, openmp, order[::-1],
+                         chunk, half_reduce)
+
+    def scan_unscale_after_flag(grad_chunks, dtype, lay, inv_scale, want_sumsq, openmp=False,
+                                ranks=None, chunk=1 << 24, half_reduce=False):
+        flag, total = False, 0.0
+        for r in (range(lay.world) if ranks is None else ranks):
+            acc = (0.0, 0.0)
+            for fs, ln in lay.segments[r]:
+                for c0 in range(fs, fs + ln, chunk):
+                    n = min(chunk, fs + ln - c0)
+                    g = oracle.reduce_sum(grad_chunks(r, c0, n), dtype, 0, n, openmp, half_reduce)
+                    flag = flag or oracle.any_nonfinite(g, openmp)
+                    if want_sumsq:
+                        acc = oracle.sumsq(g, acc)
+                    oracle.unscale(g, inv_scale, openmp)  # too late
+            total = total + oracle.sumsq_value(acc)
+        return flag, total
+
+    def window_clip_from_previous_state(grads, dtype, cfg, st, flag, total_sumsq, master, m, v,
+                                        half_reduce=False):
+        g = oracle.reduce_sum(grads, dtype, 0, master.size, half_reduce=half_reduce)
+        oracle.unscale(g, oracle.f32(1.0 / st.loss_scale))
+        if flag:
+            return None
+        if cfg.max_grad_norm > 0 and st.coef < 1.0:  # the last step's coefficient
+            oracle.scale(g, st.coef)
+        oracle.adam(g, master, m, v, oracle.step_scalars(cfg, st))
+        return oracle.f32_to_half(master, dtype)
+
     orig_scalars = oracle.step_scalars
     orig_layout = oracle.layout
+    orig_scan = oracle.scan_scalars
     return [("no bias correction", "step_scalars", no_bias_correction),
             ("stale t in bias correction", "step_scalars", stale_t),
             ("skip keeps loss scale", "skip", skip_no_backoff),
             ("commit forgets t", "commit", commit_no_t),
             ("clip without sqrt", "clip_coef", clip_no_sqrt),
-            ("floor partition", "layout", layout_floor)]
+            ("floor partition", "layout", layout_floor),
+            ("scan takes the ranks out of order", "scan_scalars", scan_ranks_reversed),
+            ("scan unscales after the flag and norm", "scan_scalars", scan_unscale_after_flag),
+            ("window clips with the last step's coefficient", "window_step",
+             window_clip_from_previous_state)]
 
 
-@pytest.mark.parametrize("idx", range(6))
+@pytest.mark.parametrize("idx", range(9))
 def test_python_mutation_is_caught(idx, monkeypatch):
     name, attr, fn = _py_mutations()[idx]
     monkeypatch.setattr(oracle, attr, fn)
