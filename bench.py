@@ -89,6 +89,8 @@ def dominant_kernel(wl) -> str:
     clip = wl.max_grad_norm > 0
     if wl.micro_steps > 1:
         return "step_kernel (accumulate passes, then the step from the accumulator)"
+    if wl.per_bucket and clip:
+        return "step_kernel (two passes, each one launch per bucket on two streams, then the commit)"
     if wl.per_bucket:
         base = ("staged_fused_kernel" if wl.rank is None and not wl.half_reduce
                 and not wl.offload_state and wl.world == 16 else "step_kernel")
@@ -397,21 +399,37 @@ def run_ours(args, wl):
             for k in range(micro):
                 z.accumulate(grads, k > 0, stream)
             z.step_accumulated(stream)
-        elif wl.per_bucket:  # one launch per bucket, alternating streams, then the commit
-            go = torch.cuda.Event()
-            go.record(stream)
-            for st in side:
-                st.wait_event(go)
-            for b in range(L.num_buckets):
-                z.step_buckets(grads, b, 1, side[b % 2])
-                if b == 0:
-                    e = torch.cuda.Event(enable_timing=True)
-                    e.record(side[0])
-                    first_bucket_done.append(e)
-            for st in side:
-                e = torch.cuda.Event()
-                e.record(st)
-                stream.wait_event(e)
+        elif wl.per_bucket:  # one launch per bucket (per pass), alternating streams, then the commit
+            def fork():
+                go = torch.cuda.Event()
+                go.record(stream)
+                for st in side:
+                    st.wait_event(go)
+
+            def join():
+                for st in side:
+                    e = torch.cuda.Event()
+                    e.record(st)
+                    stream.wait_event(e)
+
+            def buckets(launch):
+                fork()
+                for b in range(L.num_buckets):
+                    launch(b, side[b % 2])
+                    if b == 0:  # bucket 0's parameters are final here
+                        e = torch.cuda.Event(enable_timing=True)
+                        e.record(side[0])
+                        bucket0.append(e)
+                join()
+
+            bucket0 = []
+            if clip:  # first pass on every bucket, then the second pass on every bucket
+                buckets(lambda b, st: z.pass1_buckets(grads, b, 1, st))
+                bucket0.clear()
+                buckets(lambda b, st: z.pass2_buckets(grads, b, 1, st))
+            else:
+                buckets(lambda b, st: z.step_buckets(grads, b, 1, st))
+            first_bucket_done.extend(bucket0)
             z.commit(stream)
         else:
             z.step(grads, stream)
@@ -468,9 +486,10 @@ def run_ours(args, wl):
     launches_per_step = (2 if clip else 1) + (wl.micro_steps if wl.micro_steps > 1 else 0)
     pipeline = {}
     if wl.per_bucket:
-        launches_per_step = L.num_buckets + 1
+        launches_per_step = (2 if clip else 1) * L.num_buckets + 1
         firsts = [a.elapsed_time(f) for (a, _), f in zip(ev, first_bucket_done)]
         pipeline = {"pipeline": {"buckets": L.num_buckets, "streams": 2,
+                                 "passes": 2 if clip else 1,
                                  "first_bucket_ready_ms": statistics.median(firsts),
                                  "note": "time from the step's start until the first bucket's "
                                          "parameters are final (an all-gather could start)"}}

@@ -57,7 +57,9 @@
  *    others are host pointers read during the call only.
  *  - Device work is enqueued on `stream` (NULL = the legacy default stream)
  *    and runs asynchronously; nothing synchronises the host.  Calls that use
- *    the same workspace or state must be ordered on one stream.
+ *    the same workspace or state must be ordered (one stream, or events),
+ *    except the bucket-range calls of one step, which may run concurrently
+ *    as their descriptions say.
  *  - Arguments are validated on the host before anything is enqueued; on an
  *    error nothing is enqueued.  Return values: ZERO_OK (0) or a negative
  *    code below.  A value <= ZERO_ECUDA_BASE is ZERO_ECUDA_BASE - cudaError_t
@@ -182,7 +184,8 @@ typedef struct {
 /* Human-readable text for a return code (static storage). */
 ZERO_API const char *zero_strerror(int code);
 
-/* ABI version: 1. */
+/* ABI version: 2 (zero_workspace_bytes takes the layout; the clipped step's
+ * bucket-range passes). */
 ZERO_API int zero_version(void);
 
 /*
@@ -206,9 +209,22 @@ ZERO_API int zero_partition_layout(int n_tensors, const int64_t *numel, int worl
  * 1, loss_scale (a positive power of two), clip_coef 1, everything else 0. */
 ZERO_API int zero_state_init(zero_step_state *host_state, float loss_scale);
 
-/* Bytes of workspace the device-side reductions need for a group of `world`
- * ranks (a few tens of KB).  Its contents need no initialisation. */
-ZERO_API size_t zero_workspace_bytes(int world);
+/*
+ * Bytes of device workspace a step on `layout` needs (zero_step_fused,
+ * zero_step_fused_accumulated, zero_step_buckets_pass1 / _pass2), or, with
+ * layout = NULL, the bytes zero_grad_norm needs for a vector of any length
+ * (268,544).  0 for an invalid layout.
+ * The workspace holds the tree over which the global sum of squares is
+ * formed: chunks of at least 4096 elements of one rank's slice of one bucket
+ * (about 32768 chunks per rank for large partitions), 64 chunks to a
+ * superchunk, then ranks; its size is about 8 bytes per 4096 elements (a
+ * few MB for billions of parameters).  Its shape depends only on the layout,
+ * so the sum's bits do not depend on the GPU, the grid, or how the buckets
+ * are split into ranges.  It also holds counters: ZERO-FILL THE WORKSPACE
+ * ONCE before its first use; every call that runs to completion leaves the
+ * counters at zero again.
+ */
+ZERO_API size_t zero_workspace_bytes(const zero_layout *layout);
 
 /*
  * Page-locked host memory for the buffers a step exchanges with the host:
@@ -262,11 +278,16 @@ ZERO_API int zero_check_overflow(const float *g, int64_t n, float inv_scale, int
                                  zero_stream_t stream);
 
 /*
- * Step (a5): *sumsq_dev = sum over j < n of (g[j] * inv_scale)^2, accumulated
- * beyond binary64 accuracy (exact squares, compensated sums) in an order fixed
- * by n and the device, so repeated calls give the same bits.  g: device;
+ * Step (a5): *sumsq_dev = sum over j < n of (g[j] * inv_scale)^2.  The
+ * squares are formed exactly and summed in pairs of binary32 values (about
+ * 48 significant bits) within chunks, then in binary64 over a fixed tree
+ * (see zero_workspace_bytes): the order depends on n only, so every GPU and
+ * every call give the same bits, and for g a rank's reduced gradient of an
+ * unbucketed layout the result is that rank's sum in the fused step's tree.
+ * Relative error about 1e-13 or better.  g: device, 32-byte aligned;
  * sumsq_dev: device double; ws: device workspace of ws_bytes >=
- * zero_workspace_bytes(1).
+ * zero_workspace_bytes(NULL), zero-filled before its first use (the call
+ * leaves its counters at zero).  One launch (none for n = 0: *sumsq_dev = 0).
  * Pages: "zero-optimizer", "一. 优化前" (gradient-norm computation over fused
  * buffers); the clip rule itself is a reading (see zero_adam_cfg).
  */
@@ -318,22 +339,22 @@ ZERO_API int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
  * there although the framework has free memory), and loops that cannot
  * afford the device-wide synchronisation cudaMalloc and cudaFree can cause.
  * This entry point allocates nothing and calls no allocating routine.
- *  Result, arguments and summation order: as zero_grad_norm (same kernels,
- *  same grid, so the same bits), without ws / ws_bytes.
- *  Scratch: the per-CTA partial sums live in a library-owned static device
- *  array of ZERO_NOALLOC_PARTIALS doubles (32 KiB) that every GPU which
- *  loads the library holds until the process exits.  A call that would need
- *  more partial sums than that returns ZERO_ESPACE (the grid of the
- *  reduction is capped at ZERO_NOALLOC_PARTIALS CTAs, so no length of g is
- *  rejected on current GPUs).  Every call writes each slot it reads, so
- *  nothing has to be cleared between calls; but all calls share the array,
- *  so calls that can overlap on the GPU (different streams, or different
- *  host threads, without ordering between them) race and must not be issued.
+ *  Result, arguments and summation order: as zero_grad_norm (the same kernel
+ *  and the same tree, so the same bits), without ws / ws_bytes.
+ *  Scratch: the tree lives in a library-owned static device array of
+ *  ZERO_NOALLOC_SCRATCH_BYTES (268,544 bytes: the tree of a vector of any
+ *  length) that every GPU which loads the library holds until the process
+ *  exits.  A vector whose tree would not fit is rejected with ZERO_ESPACE
+ *  (none is: the chunks grow with the vector).  The array's counters are zero
+ *  when the library is loaded and every call returns them to zero; the other
+ *  slots are written before they are read.  All calls share the array, so
+ *  calls that can overlap on the GPU (different streams, or different host
+ *  threads, without ordering between them) race and must not be issued.
  *  Set-up: the first call on each device looks up the array's device
  *  address for the current device (cudaGetSymbolAddress) and caches it; make
  *  that first call before any stream capture.
  */
-#define ZERO_NOALLOC_PARTIALS 4096
+#define ZERO_NOALLOC_SCRATCH_BYTES 268544
 ZERO_API int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *sumsq_dev,
                                     zero_stream_t stream);
 
@@ -385,7 +406,9 @@ ZERO_API int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state
  *    pass drops the lines it no longer needs from L2 without writing back
  *    any that are still dirty).
  *  state_dev: device step state.  ws: device workspace of ws_bytes >=
- *    zero_workspace_bytes(layout->world).
+ *    zero_workspace_bytes(layout), zero-filled before its first use (the
+ *    clipped step's first pass forms the global sum of squares over the
+ *    workspace's fixed tree, rank by rank, then the ranks in ascending order).
  * Offload: master, m and v (all six slots) may instead be
  *  pinned host memory (cudaHostAlloc / cudaHostRegister) that the GPU reads
  *  and writes over the host link while gradients and parameters stay in
@@ -441,6 +464,59 @@ ZERO_API int zero_step_fused_buckets(const void *const *grads, int grads_are_sli
                                      float *const v[2], void *const params[2],
                                      const zero_adam_cfg *cfg, zero_step_state *state_dev,
                                      zero_stream_t stream);
+
+/*
+ * The CLIPPED step (cfg->max_grad_norm > 0) on ranges of buckets, in two
+ * passes with one global norm between them:
+ *   1. zero_step_buckets_pass1 on every bucket of the layout, exactly once,
+ *      in ranges [first_bucket, first_bucket + n_buckets): (a2) reduce, (a3)
+ *      unscale, (a4) flag NaN/Inf in state_dev->found_inf, (a5) the squares'
+ *      sums into the workspace's fixed tree, and, with g_stage, keep the
+ *      unscaled gradient there.  A range can run as soon as its buckets'
+ *      gradients are ready (during the backward pass), and ranges may run
+ *      concurrently on different streams.  The launch that completes the
+ *      tree's last superchunk (whichever range that is) adds the ranks' sums
+ *      in ascending rank order and stores the total in the workspace.
+ *   2. zero_step_buckets_pass2 on every bucket, exactly once, in ranges,
+ *      each on a stream ordered after EVERY pass-1 range: (a5) the clip with
+ *      c = min(1, max_norm / (sqrt(total) + 1e-6)), (a6) Adam/AdamW, (a7) the
+ *      cast; a range's parameters are final (ready for its all-gather) as
+ *      soon as the range completes.  Skipped (nothing written) when pass 1
+ *      flagged NaN/Inf.  The ranges may run concurrently.
+ *   3. zero_step_finalize(cfg, state_dev, 1, stream) after every pass-2 range:
+ *      commits (t + 1, cur toggled) or skips the step.
+ * The result is bit for bit that of zero_step_fused with the clip on the
+ * same buffers, whatever the split into ranges, and state_dev->sumsq /
+ * clip_coef are set as zero_step_fused sets them.  This is DeepSpeed's
+ * overlap of the optimizer step with the parameter all-gather ("DeepSpeed
+ * ZeRO", ZeRO Stage 1, 通信与计算重叠) over constant-size buffers
+ * ("相关分析", Constant Size Buffer), with the gradient norm of the page
+ * "zero-optimizer" ("一. 优化前") taken over all buckets before any update.
+ *  Arguments as zero_step_fused_buckets, plus:
+ *  g_stage: NULL, or a device fp32 buffer with the length of master (the
+ *    whole layout's, not the range's): pass 1 writes the range's unscaled
+ *    gradient there and pass 2 reads it.  Pass 2 takes exactly one source:
+ *    grads (reduced again) or g_stage.
+ *  ws, ws_bytes: the step's workspace (zero_workspace_bytes(layout),
+ *    zero-filled before first use), the same for every range of the step.
+ *  master/m/v/params (pass 2): ping-pong slots as zero_step_fused; they may
+ *    alias (in place), and must be device memory.
+ * Every bucket must go through each pass exactly once per step: a bucket left
+ * out of pass 1 leaves the tree's counters short, and no total is formed.
+ */
+ZERO_API int zero_step_buckets_pass1(const void *const *grads, int grads_are_slices,
+                                     zero_dtype dtype, const zero_layout *layout, int rank,
+                                     int64_t first_bucket, int64_t n_buckets, float *g_stage,
+                                     const zero_adam_cfg *cfg, zero_step_state *state_dev,
+                                     void *ws, size_t ws_bytes, zero_stream_t stream);
+ZERO_API int zero_step_buckets_pass2(const void *const *grads, int grads_are_slices,
+                                     zero_dtype dtype, const zero_layout *layout, int rank,
+                                     int64_t first_bucket, int64_t n_buckets,
+                                     float *const master[2], float *const m[2],
+                                     float *const v[2], void *const params[2],
+                                     const float *g_stage, const zero_adam_cfg *cfg,
+                                     zero_step_state *state_dev, const void *ws,
+                                     size_t ws_bytes, zero_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -76,7 +76,7 @@ class Workload:
     micro_steps: int = 1                 # gradient-accumulation micro-steps per step
     half_reduce: bool = False            # reduce in the gradients' half type, not fp32
     offload_state: bool = False          # master/m/v in pinned host memory
-    per_bucket: bool = False             # one launch per bucket on two streams, then the commit
+    per_bucket: bool = False             # one launch per bucket (per pass) on two streams, then the commit
 
     @property
     def numel(self) -> int:
@@ -169,5 +169,13 @@ BUCKET_CFG3 = CFG3.replace(name="flat-1.5B-nd16-fp16-bucket25M", bucket=25_000_0
 PERBUCKET_CFG3 = BUCKET_CFG3.replace(name="flat-1.5B-nd16-fp16-bucket25M-perbucket",
                                      per_bucket=True)
 
+# The 8B clipped workload run bucket by bucket: the first pass on each of the
+# 322 buckets (one launch each, alternating between two streams), then the
+# second pass on each bucket in the same way, then the commit; bucket 0's
+# parameters are final once its second pass ends.
+PERBUCKET_CFG5 = CFG5.replace(name="8B-decoder-nd8-bf16-bucket25M-clip-perbucket",
+                              per_bucket=True)
+
 BY_NAME = {w.name: w for w in ALL + (PROFILE_CFG3, PROFILE_CFG4, ACCUM_CFG3, HALFRED_CFG3,
-                                     OFFLOAD_CFG3, BUCKET_CFG3, PERBUCKET_CFG3)}
+                                     OFFLOAD_CFG3, BUCKET_CFG3, PERBUCKET_CFG3,
+                                     PERBUCKET_CFG5)}

@@ -35,7 +35,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(zs):
     names = declared_functions()
-    assert len(names) == 17, names
+    assert len(names) == 19, names
     so = ctypes.CDLL(zs._build.LIB)
     for n in names:
         assert hasattr(so, n), n
@@ -91,6 +91,41 @@ def test_bucket_step_validates_before_launch(zs):
         assert call(first, n) == E.EINVAL, (first, n)
     assert call(0, 1, w=same) == E.EINVAL
     assert call(3, 0) == E.OK and call(7, 0) == E.OK
+
+
+def test_clipped_range_passes_validate_before_launch(zs):
+    """The clipped step's range passes reject an unclipped config, ranges
+    outside the layout, a second pass with both or neither gradient source,
+    misaligned stages and a small workspace before anything is enqueued; a
+    zero-bucket range enqueues nothing."""
+    lib = zs._abi.lib()
+    E = zs._abi
+    lay, _ = zs.zero_partition_layout([100_000, 3], 2, bucket_numel=2 * 8 * 1024)
+    fake = 1 << 20
+    g2 = (ctypes.c_void_p * 2)(fake, fake)
+    slots = (ctypes.c_void_p * 2)(fake, fake + 4096)
+    clip = zs.adam_cfg(max_grad_norm=1.0)
+    wsb = zs.zero_workspace_bytes(lay)
+
+    def p1(first, n, cfg=clip, stage=None, ws_bytes=wsb, grads=g2):
+        return lib.zero_step_buckets_pass1(grads, 0, 0, ctypes.byref(lay), -1, first, n, stage,
+                                           ctypes.byref(cfg), fake, fake, ws_bytes, None)
+
+    def p2(first, n, cfg=clip, stage=None, grads=g2, ws_bytes=wsb):
+        return lib.zero_step_buckets_pass2(grads, 0, 0, ctypes.byref(lay), -1, first, n, slots,
+                                           slots, slots, slots, stage, ctypes.byref(cfg), fake,
+                                           fake, ws_bytes, None)
+
+    assert p1(0, 1, zs.adam_cfg()) == E.EINVAL and p2(0, 1, zs.adam_cfg()) == E.EINVAL
+    for first, n in ((-1, 1), (0, -1), (7, 1), (6, 2)):
+        assert p1(first, n) == E.EINVAL and p2(first, n) == E.EINVAL, (first, n)
+    assert p1(0, 1, grads=None) == E.EINVAL
+    assert p2(0, 1, stage=fake) == E.EINVAL          # both sources
+    assert p2(0, 1, grads=None) == E.EINVAL          # neither
+    assert p1(0, 1, stage=fake + 16) == E.EALIGN
+    assert p2(0, 1, grads=None, stage=fake + 16) == E.EALIGN
+    assert p1(0, 1, ws_bytes=wsb - 8) == E.ESPACE and p2(0, 1, ws_bytes=wsb - 8) == E.ESPACE
+    assert p1(4, 0) == E.OK and p2(4, 0) == E.OK
 
 
 def test_structs_match_header(tmp_path, zs):
@@ -165,9 +200,42 @@ def test_state_init_and_workspace(zs):
     st = zs.StepState()
     for bad in (0.0, -2.0, 3.0, float("inf"), float("nan")):
         assert lib.zero_state_init(ctypes.byref(st), bad) == zs._abi.EINVAL
-    assert zs.zero_workspace_bytes(1) >= 256 + 8 * 4096
-    assert lib.zero_workspace_bytes(0) == 0 and lib.zero_workspace_bytes(1025) == 0
+    assert zs.zero_workspace_bytes() == zs._abi.NOALLOC_SCRATCH_BYTES == 268544
+    broken = zs.zero_partition_layout([1000], 2)[0]
+    broken.owned_numel += 8
+    assert lib.zero_workspace_bytes(ctypes.byref(broken)) == 0
     assert lib.zero_strerror(zs._abi.EALIGN).decode().startswith("buffer")
+
+
+def _tree_bytes(world, slice_units, last_units, nb):
+    """The norm tree's workspace bytes, computed from its definition: chunks
+    of at least 512 units (a multiple of 256) sized so a rank has about
+    32768 of them, restarting at every bucket slice; 64 chunks per
+    superchunk; a 256-byte header, then a 4-byte counter per superchunk
+    (padded to 256 bytes), then a double per chunk and per superchunk."""
+    cd = lambda a, b: -(-a // b)
+    units = (nb - 1) * slice_units + last_units
+    cu = max(512, cd(cd(units, 32768), 256) * 256)
+    cps_last = cd(last_units, cu)
+    cps = cd(slice_units, cu) if nb > 1 else cps_last
+    cpr = (nb - 1) * cps + cps_last
+    spr = cd(cpr, 64)
+    return 256 + cd(world * spr * 4, 256) * 256 + 8 * world * cpr + 8 * world * spr
+
+
+@pytest.mark.parametrize("wl", ALL, ids=lambda w: w.name)
+def test_workspace_holds_the_norm_tree(zs, wl):
+    """zero_workspace_bytes(layout) is the size of the norm's tree for every
+    rank of the layout: about 8 bytes per 4096 elements (2.1 MB for the 8B
+    decoder over 8 ranks)."""
+    lay, _ = zs.zero_partition_layout(wl.numels, wl.world, 64, wl.bucket)
+    if wl.bucket:
+        want = _tree_bytes(wl.world, lay.slice_numel // 8, lay.last_slice_numel // 8,
+                           lay.num_buckets)
+    else:
+        want = _tree_bytes(wl.world, lay.owned_numel // 8, lay.owned_numel // 8, 1)
+    assert zs.zero_workspace_bytes(lay) == want
+    assert want <= lay.padded_numel // 400 + (1 << 16)
 
 
 def test_entry_points_validate_before_launch(zs):

@@ -16,7 +16,8 @@ import torch
 
 import oracle
 import synth
-from synth.workloads import CFG2, CFG3, CFG4, CFG5, OFFLOAD_CFG3, PERBUCKET_CFG3
+from synth.workloads import (CFG2, CFG3, CFG4, CFG5, OFFLOAD_CFG3, PERBUCKET_CFG3,
+                             PERBUCKET_CFG5)
 import zero_partitioned_mixed_step_gb300 as zs
 from zs_harness import (INF_BITS, SUMSQ_RTOL, assert_close, assert_half_close, half_bits,
                         lib_cfg, oracle_cfg)
@@ -169,25 +170,56 @@ def flat_of_local(lay, r, k, n):
     raise AssertionError("window outside the rank")
 
 
-def step_group(z, grads, wl):
+def _ws_total(z):
+    """The sum of squares the last first pass left in the workspace (bytes 8-15)."""
+    return bytes(z.ws[8:16].cpu().numpy().tobytes())
+
+
+def step_group(z, grads, wl, check_split=False):
     """The step as the benchmark launches it: one fused call, or (per-bucket
-    workloads) one call per bucket alternating between two streams, then the
-    commit."""
+    workloads) one call per bucket (per pass with the clip) alternating
+    between two streams, then the commit.  check_split: before the clipped
+    per-bucket first pass, run it once as a single range over all buckets
+    and require the same total bits from the split run."""
     if not wl.per_bucket:
         z.step(grads)
         return
     s0 = torch.cuda.current_stream()
     side = [torch.cuda.Stream(), torch.cuda.Stream()]
-    go = torch.cuda.Event()
-    go.record(s0)
-    for st in side:
-        st.wait_event(go)
-    for b in range(z.layout.num_buckets):
-        z.step_buckets(grads, b, 1, side[b % 2])
-    for st in side:
-        done = torch.cuda.Event()
-        done.record(st)
-        s0.wait_event(done)
+    nb = z.layout.num_buckets
+
+    def fork():
+        go = torch.cuda.Event()
+        go.record(s0)
+        for st in side:
+            st.wait_event(go)
+
+    def join():
+        for st in side:
+            done = torch.cuda.Event()
+            done.record(st)
+            s0.wait_event(done)
+
+    if wl.max_grad_norm > 0:
+        whole = None
+        if check_split:
+            z.pass1_buckets(grads, 0, nb, s0)
+            whole = _ws_total(z)
+        fork()
+        for b in range(nb):
+            z.pass1_buckets(grads, b, 1, side[b % 2])
+        join()
+        if check_split:
+            assert _ws_total(z) == whole
+        fork()
+        for b in range(nb):
+            z.pass2_buckets(grads, b, 1, side[b % 2])
+        join()
+    else:
+        fork()
+        for b in range(nb):
+            z.step_buckets(grads, b, 1, side[b % 2])
+        join()
     z.commit(s0)
 
 
@@ -210,7 +242,7 @@ def run_windowed(wl, steps, stage=None):
     for s in range(1, steps + 1):
         S = st.loss_scale
         grp.regen(s, S)
-        step_group(z, grp.grads, wl)
+        step_group(z, grp.grads, wl, check_split=s == 2)
         flag, sumsq = oracle.scan_scalars(grp.chunk, wl.dtype, lay, oracle.f32(1.0 / S),
                                           cfg.max_grad_norm > 0, openmp=True, ranks=ranks)
         for key, (w, m, v, h) in state.items():
@@ -286,6 +318,19 @@ def test_fullsize_8B_buckets_clip():
         pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
     st = run_windowed(CFG5, steps=2, stage=True)
     assert st.t == 2
+
+
+def test_fullsize_8B_buckets_clip_per_bucket():
+    """The same workload as the clipped step on bucket ranges: the first pass
+    on each of the 322 buckets (two streams), then the second pass on each,
+    then the commit; in step 2 the first pass also runs once over all
+    buckets, and the split run's total has the same bits."""
+    free, _ = torch.cuda.mem_get_info()
+    need = 8 * 8_030_261_248 * 2 + 8_030_261_248 * (12 + 2 + 4) + (2 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+    st = run_windowed(PERBUCKET_CFG5, steps=2, stage=True)
+    assert st.t == 2 and st.coef < 1.0
 
 
 def test_fullsize_gpt2_nd8_clip_every_element():

@@ -214,7 +214,7 @@ def test_unfused_entry_points_match_oracle_and_fused():
     zs.zero_check_overflow(odd, 1.0, flag.data_ptr())
     assert int(flag.item()) == 1
     # (a5)
-    ws = torch.empty(zs.zero_workspace_bytes(wl.world), dtype=torch.uint8, device=dev)
+    ws = zs.new_workspace()
     zs.zero_grad_norm(g_all, 1.0, zs.state_field_ptr(state, "sumsq"), ws)
     s = zs.read_state(state).sumsq
     ref = oracle.sumsq_value(oracle.sumsq(want))
@@ -488,36 +488,24 @@ def test_staged_path_matches_register_path(world, dtype):
 
 def test_staged_wait_that_runs_out_skips_the_step_and_reports():
     """Every mbarrier wait of the shared-memory staged kernel is bounded.
-    With ZERO_TEST_STAGED_WAIT_LIMIT set, each stage is announced 16 bytes
-    more than its copies bring, so every CTA's first wait runs out after 1000
-    polls: the kernel records state.error, skips the step (every buffer's
-    current slot unchanged bit for bit, the dynamic loss scale backed off),
-    retires the extra bytes, waits for its own copies and finishes.  With the
-    error cleared, the next step commits in lockstep with the oracle."""
-    wl = CFG1.replace(numels=(200_001,), world=16, steps=3, inject_at=(), dynamic_scale=True)
-    ls = Lockstep(wl)
-    ls.step()
-    ls.check()
-    before = [t.clone() for t in ls.z.current()]
-    grads = gen_grads(wl, ls.lay, 2, ls.st.loss_scale)
-    os.environ["ZERO_TEST_STAGED_WAIT_LIMIT"] = "1000"
-    try:
-        ls.z.step([to_dev_half(g, wl.dtype) for g in grads])
-        torch.cuda.synchronize()
-    finally:
-        del os.environ["ZERO_TEST_STAGED_WAIT_LIMIT"]
-    st = ls.z.read_state()
-    assert (st.error, st.overflow, st.skipped, st.t, st.found_inf) == (1, 1, 1, 1, 0)
-    assert st.loss_scale == wl.loss_scale / 2
-    for a, b in zip(before, ls.z.current()):
-        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
-    oracle.skip(ls.ocfg, ls.st)  # the oracle's view of the same step
-    ls.steps += 1
-    off = zs.StepState.error.offset
-    ls.z.state[off:off + 4].zero_()  # the caller has handled the error
-    ls.step()
-    st = ls.check()
-    assert st.t == 2 and st.skipped == 1
+    With ZERO_TEST_STAGED_WAIT_LIMIT set (read once per process, so the
+    check runs in a child process: tests/gpu_children.py), each stage is
+    announced 16 bytes more than its copies bring, so every CTA's first wait
+    runs out after 1000 polls: the kernel records state.error, skips the step
+    (every buffer's current slot unchanged bit for bit, the dynamic loss
+    scale backed off), retires the extra bytes, waits for its own copies and
+    finishes; a second step does the same, and the process then keeps using
+    the GPU."""
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, ZERO_TEST_STAGED_WAIT_LIMIT="1000")
+    env.pop("ZERO_TEST_MAX_CTAS", None)
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "gpu_children.py"), "staged_wait"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert json.loads(r.stdout.strip().splitlines()[-1]) == {"ok": True}
 
 
 GRAPHED = {

@@ -8,7 +8,10 @@ used for device memory, streams and pinned host memory.
 Entry points (same names as the C ABI):
   zero_partition_layout, zero_state_init, zero_workspace_bytes,
   zero_reduce_scatter_sum, zero_check_overflow, zero_grad_norm,
-  zero_adam_step, zero_step_finalize, zero_step_fused.
+  zero_grad_norm_noalloc, zero_adam_step, zero_step_finalize,
+  zero_step_fused, zero_reduce_scatter_accumulate,
+  zero_step_fused_accumulated, zero_step_fused_buckets,
+  zero_step_buckets_pass1, zero_step_buckets_pass2.
 ``ZeroStep`` owns the buffers of one simulated data-parallel group and runs
 the fused step on them.
 """
@@ -25,11 +28,11 @@ HALF_REDUCE = 2  # added to F16 / BF16: reduce in the half type instead of fp32
 
 __all__ = [
     "F16", "BF16", "MAX_WORLD", "AdamCfg", "Layout", "StepState", "ZeroError", "ZeroStep",
-    "adam_cfg", "new_state", "read_state", "state_field_ptr", "zero_partition_layout",
+    "adam_cfg", "new_state", "new_workspace", "read_state", "state_field_ptr", "zero_partition_layout",
     "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
     "zero_grad_norm", "zero_grad_norm_noalloc", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
     "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated", "zero_step_fused_buckets",
-    "host_empty",
+    "zero_step_buckets_pass1", "zero_step_buckets_pass2", "host_empty",
 ]
 
 _TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
@@ -102,11 +105,19 @@ def zero_state_init(loss_scale: float = 1.0) -> StepState:
     return s
 
 
-def zero_workspace_bytes(world: int) -> int:
-    n = lib().zero_workspace_bytes(world)
+def zero_workspace_bytes(layout: Optional[Layout] = None) -> int:
+    """Workspace bytes of a step on `layout` (zero-fill it before first use),
+    or with no layout the bytes zero_grad_norm needs."""
+    n = lib().zero_workspace_bytes(ctypes.byref(layout) if layout is not None else None)
     if n == 0:
         raise ZeroError("zero_workspace_bytes", -1)
     return n
+
+
+def new_workspace(layout: Optional[Layout] = None, device="cuda") -> torch.Tensor:
+    """A zero-filled device workspace for steps on `layout` (or for
+    zero_grad_norm with no layout)."""
+    return torch.zeros(zero_workspace_bytes(layout), dtype=torch.uint8, device=device)
 
 
 class _HostBlock:
@@ -247,6 +258,48 @@ def zero_step_fused_buckets(grads: Sequence[torch.Tensor], layout: Layout, first
                                         ctypes.byref(cfg), _dev_ptr(state), _stream(stream)))
 
 
+def zero_step_buckets_pass1(grads: Sequence[torch.Tensor], layout: Layout, first_bucket: int,
+                            n_buckets: int, cfg: AdamCfg, state: torch.Tensor, ws: torch.Tensor,
+                            rank: int = -1, g_stage: Optional[torch.Tensor] = None,
+                            grads_are_slices: bool = False, stream=None,
+                            half_reduce: bool = False) -> None:
+    """First pass of the clipped step on buckets [first_bucket, first_bucket
+    + n_buckets): reduce, unscale, flag, the squares into the workspace's
+    tree (and the unscaled gradient into g_stage when given)."""
+    check("zero_step_buckets_pass1",
+          lib().zero_step_buckets_pass1(_grad_array(grads), int(grads_are_slices),
+                                        _grad_code(grads, half_reduce), ctypes.byref(layout),
+                                        rank, first_bucket, n_buckets, _dev_ptr(g_stage),
+                                        ctypes.byref(cfg), _dev_ptr(state), _dev_ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def zero_step_buckets_pass2(grads: Optional[Sequence[torch.Tensor]], layout: Layout,
+                            first_bucket: int, n_buckets: int, master: Sequence[torch.Tensor],
+                            m: Sequence[torch.Tensor], v: Sequence[torch.Tensor],
+                            params: Sequence[torch.Tensor], cfg: AdamCfg, state: torch.Tensor,
+                            ws: torch.Tensor, rank: int = -1,
+                            g_stage: Optional[torch.Tensor] = None, dtype: Optional[int] = None,
+                            grads_are_slices: bool = False, stream=None,
+                            half_reduce: bool = False) -> None:
+    """Second pass of the clipped step on a range of buckets: clip, Adam,
+    cast; the gradient is reduced again (grads) or read from g_stage."""
+    if grads is not None:
+        code = _grad_code(grads, half_reduce)
+        garr = _grad_array(grads)
+    else:
+        code = (dtype if dtype is not None else _dtype_code(params[0])) | (
+            HALF_REDUCE if half_reduce else 0)
+        garr = None
+    check("zero_step_buckets_pass2",
+          lib().zero_step_buckets_pass2(garr, int(grads_are_slices), code, ctypes.byref(layout),
+                                        rank, first_bucket, n_buckets, _state_array(master),
+                                        _state_array(m), _state_array(v), _ptr_array(params),
+                                        _dev_ptr(g_stage), ctypes.byref(cfg), _dev_ptr(state),
+                                        _dev_ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)))
+
+
 def zero_reduce_scatter_accumulate(grads: Sequence[torch.Tensor], layout: Layout,
                                    acc: torch.Tensor, add: bool, rank: int = -1,
                                    grads_are_slices: bool = False, stream=None,
@@ -324,7 +377,7 @@ class ZeroStep:
             stage_grad = clip and world > 4
         self.g_stage = torch.empty(self.n_state, **f32) if (clip and stage_grad) else None
         self.state = new_state(loss_scale, device)
-        self.ws = torch.empty(zero_workspace_bytes(world), dtype=torch.uint8, device=device)
+        self.ws = new_workspace(self.layout, device)
 
     def segments(self, r: int) -> List[Tuple[int, int]]:
         """(flat start, length) of the ranges rank r owns, in r's element order."""
@@ -354,6 +407,24 @@ class ZeroStep:
         zero_step_fused_buckets(grads, self.layout, first_bucket, n_buckets, self.master,
                                 self.m, self.v, self.params, self.cfg, self.state, self.rank,
                                 self.grads_are_slices, stream, self.half_reduce)
+
+    def pass1_buckets(self, grads: Sequence[torch.Tensor], first_bucket: int, n_buckets: int,
+                      stream=None) -> None:
+        """The clipped step's first pass on a range of buckets."""
+        zero_step_buckets_pass1(grads, self.layout, first_bucket, n_buckets, self.cfg,
+                                self.state, self.ws, self.rank, self.g_stage,
+                                self.grads_are_slices, stream, self.half_reduce)
+
+    def pass2_buckets(self, grads: Optional[Sequence[torch.Tensor]], first_bucket: int,
+                      n_buckets: int, stream=None) -> None:
+        """The clipped step's second pass on a range of buckets (the gradient
+        from the stage when the group keeps one, else reduced again from
+        grads)."""
+        zero_step_buckets_pass2(None if self.g_stage is not None else grads, self.layout,
+                                first_bucket, n_buckets, self.master, self.m, self.v,
+                                self.params, self.cfg, self.state, self.ws, self.rank,
+                                self.g_stage, self.dtype, self.grads_are_slices, stream,
+                                self.half_reduce)
 
     def commit(self, stream=None) -> None:
         """End a step run bucket by bucket: commit, or skip on NaN/Inf."""

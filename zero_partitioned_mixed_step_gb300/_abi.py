@@ -15,7 +15,7 @@ EALIGN = -2
 ESPACE = -3
 ECUDA_BASE = -1000
 MAX_WORLD = 1024
-NOALLOC_PARTIALS = 4096
+NOALLOC_SCRATCH_BYTES = 268544
 
 
 class Layout(ctypes.Structure):
@@ -57,7 +57,7 @@ SIGNATURES = {
     "zero_partition_layout": ([_I, ctypes.POINTER(ctypes.c_int64), _I, _I, _I64,
                                ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(Layout)], _I),
     "zero_state_init": ([ctypes.POINTER(StepState), ctypes.c_float], _I),
-    "zero_workspace_bytes": ([_I], ctypes.c_size_t),
+    "zero_workspace_bytes": ([ctypes.POINTER(Layout)], ctypes.c_size_t),
     "zero_host_alloc": ([ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)], _I),
     "zero_host_free": ([_P], _I),
     "zero_reduce_scatter_sum": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _P, _P], _I),
@@ -73,6 +73,11 @@ SIGNATURES = {
                                  _P, ctypes.POINTER(AdamCfg), _P, _P], _I),
     "zero_step_fused_accumulated": ([_P, _I, ctypes.POINTER(Layout), _I, _P, _P, _P, _P,
                                      ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P], _I),
+    "zero_step_buckets_pass1": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _I64, _I64, _P,
+                                 ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P], _I),
+    "zero_step_buckets_pass2": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _I64, _I64, _P, _P, _P,
+                                 _P, _P, ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P],
+                                _I),
 }
 
 _lib = None

@@ -3,6 +3,7 @@
 // end a step.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 
 #include "kernels.cuh"
 
@@ -53,6 +54,8 @@ int resident_ctas(const void *kernel)
     return occ;
 }
 
+}  // namespace
+
 int device_sms()
 {
     int dev = 0, sms = 0;
@@ -68,12 +71,23 @@ int device_sms()
     return sms;
 }
 
-}  // namespace
+int test_grid_cap()
+{
+    static const int cap = [] {
+        const char *t = std::getenv("ZERO_TEST_MAX_CTAS");
+        const long v = t ? std::atol(t) : 0;
+        return v > 0 && v < kMaxCtas ? (int)v : 0;
+    }();
+    return cap;
+}
 
 int target_ctas(const void *kernel)
 {
-    const int64_t t = (int64_t)device_sms() * resident_ctas(kernel);
-    return (int)(t > kMaxCtas ? kMaxCtas : t);
+    int64_t t = (int64_t)device_sms() * resident_ctas(kernel);
+    if (t > kMaxCtas)
+        t = kMaxCtas;
+    const int cap = test_grid_cap();
+    return (int)(cap > 0 && t > cap ? cap : t);
 }
 
 // ------------------------------------------------------------------ end of step
@@ -88,43 +102,6 @@ __global__ void finalize_kernel(FinCfg c, zero_step_state *st, int flip)
 int launch_finalize(const zero_adam_cfg *cfg, zero_step_state *state, int flip, cudaStream_t s)
 {
     finalize_kernel<<<1, 32, 0, s>>>(fin_cfg(*cfg), state, flip);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
-}
-
-// Fixed-order reduction of per-CTA partials: warp w reduces rows w, w + 8, ...
-// (lane l adds columns l, l + 32, ... in order, then a fixed butterfly), then
-// thread 0 adds the row sums in row (rank) order.
-__global__ void __launch_bounds__(kThreads)
-    norm_finalize_kernel(const double *partials, int gx, int gy, double max_norm,
-                         zero_step_state *st, double *out)
-{
-    __shared__ double row_sum[ZERO_MAX_WORLD];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r < gy; r += kThreads / 32) {
-        const double x = warp_fixed_sum(partials + (int64_t)r * gx, gx);
-        if (lane == 0)
-            row_sum[r] = x;
-    }
-    __syncthreads();
-    if (threadIdx.x != 0)
-        return;
-    double total = 0.0;
-    for (int r = 0; r < gy; ++r)
-        total = __dadd_rn(total, row_sum[r]);
-    if (out)
-        *out = total;
-    if (st && !(st->found_inf & 1)) {
-        st->sumsq = total;
-        if (max_norm > 0.0)
-            st->clip_coef = clip_coefficient(total, max_norm);
-    }
-}
-
-int launch_norm_finalize(const double *partials, int gx, int gy, double max_norm,
-                         zero_step_state *state, double *out, cudaStream_t s)
-{
-    norm_finalize_kernel<<<1, kThreads, 0, s>>>(partials, gx, gy, max_norm, state, out);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
@@ -154,29 +131,62 @@ __global__ void __launch_bounds__(kThreads)
     flag_nonfinite(bad, flag);
 }
 
+// The sum of squares of g * inv_s over the norm's fixed tree (internal.h),
+// the vector taken as one rank's single slice of ceil(n / 8) units (the last
+// one padded with zeros); the CTA that completes the tree writes the total.
 __global__ void __launch_bounds__(kThreads)
-    sumsq_kernel(const float *g, int64_t n, float inv_s, double *partials)
+    norm_kernel(const float *g, int64_t n, float inv_s, NormPlan np)
 {
-    SumSq ss;
-    const int64_t units = n / kUnit;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < units; k += stride) {
-        float x[8];
-        load8(g + k * kUnit, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            x[i] = __fmul_rn(x[i], inv_s);
-        ss.add8(x);
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0 && (n % kUnit)) {
-        float x[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int64_t i = units * kUnit; i < n; ++i)
-            x[i - units * kUnit] = __fmul_rn(g[i], inv_s);
-        ss.add8(x);
-    }
-    const double tot = block_sum(ss.acc);
+    __shared__ NormShared nsh;
     if (threadIdx.x == 0)
-        partials[blockIdx.x] = tot;
+        nsh.final_pending = 0;
+    __syncthreads();
+    const int64_t full = n / kUnit;
+    SumSq ss;
+    int parity = 0;
+    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x, parity ^= 1) {
+        const ChunkLoc L = locate_chunk(np, pi);
+        ss.acc = FF{0.0f, 0.0f};
+        for (int64_t k = threadIdx.x; k < L.n_u; k += kThreads) {
+            const int64_t u = L.u0 + k;
+            float x[8];
+            if (u < full) {
+                load8(g + u * kUnit, x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    x[i] = u * kUnit + i < n ? g[u * kUnit + i] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                x[i] = __fmul_rn(x[i], inv_s);
+            ss.add8(x);
+        }
+        norm_chunk_done(np, L, ss.acc, parity, nsh);
+    }
+    __syncthreads();
+    norm_finish(np, nsh);
+}
+
+// zero_grad_norm's launch with the tree in `ws` (a workspace of at least
+// norm_ws_bytes_any_vector() bytes whose counters are zero).
+static int launch_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
+                       size_t ws_bytes, cudaStream_t stream)
+{
+    if (n == 0) {  // an empty sum: +0
+        const cudaError_t e = cudaMemsetAsync(sumsq_dev, 0, sizeof(double), stream);
+        return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+    }
+    const int64_t units = (n + kUnit - 1) / kUnit;
+    const NormGeom geo = norm_geometry(units, units, 1);
+    if (norm_ws_bytes(1, geo) > ws_bytes)
+        return ZERO_ESPACE;
+    const NormPlan np = norm_plan(geo, units, units, 1, 0, 1, 1, ws, sumsq_dev);
+    const int target = target_ctas(reinterpret_cast<const void *>(norm_kernel));
+    const int gx = (int)(np.launch_chunks < target ? np.launch_chunks : target);
+    norm_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, np);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
 
 template <int DT>
@@ -257,15 +267,9 @@ int zero_grad_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev
         return ZERO_EINVAL;
     if (!aligned32(g) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(sumsq_dev) & 7u))
         return ZERO_EALIGN;
-    if (ws_bytes < zero_workspace_bytes(1))
+    if (ws_bytes < zero_workspace_bytes(nullptr))
         return ZERO_ESPACE;
-    double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
-    const int gx = grid_for(reinterpret_cast<const void *>(sumsq_kernel), n / kUnit);
-    sumsq_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, partials);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return cuda_error(e);
-    return launch_norm_finalize(partials, gx, 1, 0.0, nullptr, sumsq_dev, stream);
+    return launch_norm(g, n, inv_scale, sumsq_dev, ws, ws_bytes, stream);
 }
 
 int zero_adam_step(const float *g, float *master, float *m, float *v, void *half_out,
@@ -314,40 +318,45 @@ int zero_step_finalize(const zero_adam_cfg *cfg, zero_step_state *state_dev, int
 
 // ------------------------------------------------------------------ no-allocation norm
 //
-// zero_grad_norm_noalloc: the same two kernels as zero_grad_norm, with the
-// per-CTA partial sums in a library-owned device array instead of a
-// caller-provided workspace.
+// zero_grad_norm_noalloc: zero_grad_norm's kernel with the norm's tree in a
+// library-owned device array instead of a caller-provided workspace.
 
 namespace zs {
 
-// One slot per CTA of the sum-of-squares grid.  Every GPU that loads the
-// library holds this array (ZERO_NOALLOC_PARTIALS doubles, 32 KiB) until the
-// process exits.  In host code the name is only a host-side stand-in for
-// the device array: kernels must be given the address cudaGetSymbolAddress
-// returns for the current device.
-static __device__ __align__(256) double noalloc_partials[ZERO_NOALLOC_PARTIALS];
+static_assert(kNormWsAnyVector == ZERO_NOALLOC_SCRATCH_BYTES,
+              "the static scratch holds the tree of any vector");
+
+// The tree of one call: counters (zero when the library is loaded, and
+// returned to zero by every call that completes), chunk and superchunk sums
+// and the result slot.  Every GPU that loads the library holds this array
+// until the process exits.  In host code the name is only a host-side
+// stand-in for the device array: kernels must be given the address
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char noalloc_ws[ZERO_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kNoallocDevices = 64;
-static std::atomic<double *> noalloc_ptr[kNoallocDevices];
+static std::atomic<void *> noalloc_ptr[kNoallocDevices];
 
-// The device address of noalloc_partials on device `dev` (the current
-// device), looked up on the first call for that device and cached.
-static int noalloc_scratch(int dev, double **out)
+// The device address of noalloc_ws on device `dev` (the current device),
+// looked up on the first call for that device and cached.
+static int noalloc_scratch(int dev, void **out)
 {
     if (dev >= 0 && dev < kNoallocDevices) {
-        double *p = noalloc_ptr[dev].load(std::memory_order_acquire);
+        void *p = noalloc_ptr[dev].load(std::memory_order_acquire);
         if (p) {
             *out = p;
             return ZERO_OK;
         }
     }
     void *addr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&addr, noalloc_partials);
-    if (e != cudaSuccess || !addr)
+    const cudaError_t e = cudaGetSymbolAddress(&addr, noalloc_ws);
+    if (e != cudaSuccess || !addr) {
+        (void)cudaGetLastError();
         return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    }
     if (dev >= 0 && dev < kNoallocDevices)
-        noalloc_ptr[dev].store(static_cast<double *>(addr), std::memory_order_release);
-    *out = static_cast<double *>(addr);
+        noalloc_ptr[dev].store(addr, std::memory_order_release);
+    *out = addr;
     return ZERO_OK;
 }
 
@@ -362,19 +371,16 @@ extern "C" int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale
     if (!aligned32(g) || (reinterpret_cast<uintptr_t>(sumsq_dev) & 7u))
         return ZERO_EALIGN;
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
         return cuda_error(e);
-    double *partials = nullptr;
-    int rc = noalloc_scratch(dev, &partials);
+    }
+    void *scratch = nullptr;
+    const int rc = noalloc_scratch(dev, &scratch);
     if (rc)
         return rc;
-    const int gx = grid_for(reinterpret_cast<const void *>(sumsq_kernel), n / kUnit);
-    if (gx > ZERO_NOALLOC_PARTIALS)
-        return ZERO_ESPACE;  // more CTAs than the static scratch has slots
-    sumsq_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, partials);
-    e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return cuda_error(e);
-    return launch_norm_finalize(partials, gx, 1, 0.0, nullptr, sumsq_dev, stream);
+    // a vector whose tree needs more than the array holds is ZERO_ESPACE
+    // (none does: the chunks grow with the vector)
+    return launch_norm(g, n, inv_scale, sumsq_dev, scratch, ZERO_NOALLOC_SCRATCH_BYTES, stream);
 }

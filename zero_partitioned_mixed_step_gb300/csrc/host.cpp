@@ -34,6 +34,57 @@ int check_layout(const zero_layout *lay)
     return ZERO_OK;
 }
 
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+NormGeom norm_geometry(int64_t slice_units, int64_t last_slice_units, int64_t nb)
+{
+    NormGeom g{};
+    const int64_t rank_units = (nb > 0 ? nb - 1 : 0) * slice_units + last_slice_units;
+    g.cu = round_up(ceil_div(rank_units, kNormChunksPerRank), kThreads);
+    if (g.cu < kNormChunkMinUnits)
+        g.cu = kNormChunkMinUnits;
+    g.cps_last = ceil_div(last_slice_units, g.cu);
+    g.cps = nb > 1 ? ceil_div(slice_units, g.cu) : g.cps_last;
+    g.cpr = (nb > 0 ? nb - 1 : 0) * g.cps + g.cps_last;
+    g.spr = ceil_div(g.cpr, kNormSuper);
+    return g;
+}
+
+size_t norm_ws_bytes(int64_t ranks, const NormGeom &g)
+{
+    const int64_t counters = round_up(ranks * g.spr * (int64_t)sizeof(uint32_t), 256);
+    return (size_t)(kWsHeader + counters + ranks * g.cpr * (int64_t)sizeof(double) +
+                    ranks * g.spr * (int64_t)sizeof(double));
+}
+
+NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_units, int64_t nb,
+                   int64_t b0, int64_t nbl, int32_t ranks, void *ws, double *total)
+{
+    NormPlan p{};
+    p.cu = g.cu;
+    p.cps = g.cps;
+    p.cps_last = g.cps_last;
+    p.cpr = g.cpr;
+    p.spr = g.spr;
+    p.slice_units = slice_units;
+    p.last_slice_units = last_slice_units;
+    p.nb = nb;
+    p.b0 = b0;
+    p.nbl = nbl;
+    const bool has_last = b0 + nbl == nb;
+    p.launch_chunks = (int64_t)ranks * ((nbl - (has_last ? 1 : 0)) * g.cps +
+                                        (has_last ? g.cps_last : 0));
+    p.ranks = ranks;
+    char *base = static_cast<char *>(ws);
+    p.done = reinterpret_cast<uint32_t *>(base);
+    p.sc_count = reinterpret_cast<uint32_t *>(base + kWsHeader);
+    const int64_t counters = round_up((int64_t)ranks * g.spr * (int64_t)sizeof(uint32_t), 256);
+    p.partials = reinterpret_cast<double *>(base + kWsHeader + counters);
+    p.sc_partials = p.partials + (int64_t)ranks * g.cpr;
+    p.total = total ? total : norm_total_slot(ws);
+    return p;
+}
+
 static bool power_of_two(double x)
 {
     int e;
@@ -71,7 +122,7 @@ const char *zero_strerror(int code)
     }
 }
 
-int zero_version(void) { return 1; }
+int zero_version(void) { return 2; }
 
 int zero_partition_layout(int n_tensors, const int64_t *numel, int world, int align_elems,
                           int64_t bucket_numel, int64_t *tensor_offset_out, zero_layout *out)
@@ -136,11 +187,18 @@ int zero_state_init(zero_step_state *s, float loss_scale)
     return ZERO_OK;
 }
 
-size_t zero_workspace_bytes(int world)
+size_t zero_workspace_bytes(const zero_layout *layout)
 {
-    if (world < 1 || world > ZERO_MAX_WORLD)
+    if (!layout)
+        return zs::norm_ws_bytes_any_vector();
+    if (zs::check_layout(layout))
         return 0;
-    return (size_t)zs::kWsHeader + sizeof(double) * (size_t)(zs::kMaxCtas + 2 * world);
+    const zero_layout &L = *layout;
+    const int64_t nb = L.bucket_numel ? L.num_buckets : (L.padded_numel ? 1 : 0);
+    const int64_t su = (L.bucket_numel ? L.slice_numel : L.owned_numel) / zs::kUnit;
+    const zs::NormGeom g = zs::norm_geometry(su, L.last_slice_numel / zs::kUnit, nb);
+    const size_t need = zs::norm_ws_bytes(L.world, g);
+    return need > (size_t)zs::kWsHeader ? need : (size_t)zs::kWsHeader;
 }
 
 int zero_host_alloc(size_t bytes, void **out)
@@ -150,7 +208,8 @@ int zero_host_alloc(size_t bytes, void **out)
     *out = nullptr;
     if (bytes == 0)
         return ZERO_OK;
-    const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocDefault);
+    // portable: page-locked for every device's context, not only the current one
+    const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocPortable | cudaHostAllocMapped);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         *out = nullptr;

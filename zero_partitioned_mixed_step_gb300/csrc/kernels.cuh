@@ -491,13 +491,35 @@ __device__ __forceinline__ uint16_t round_half1(float w)
 }
 
 // ------------------------------------------------------------------ sum of squares
+//
+// Squares are summed in pairs of binary32 values (hi, lo) whose sum carries
+// about 48 significant bits, without binary64 arithmetic in the streaming
+// loops (GB300 issues binary64 at a small fraction of the binary32 rate):
+// each square is split exactly into p + e (p = fl(g*g), e = fma(g, g, -p)),
+// a unit's p are added with Knuth's TwoSum so their rounding errors are kept,
+// and pairs are added with a TwoSum on the high parts followed by a
+// renormalisation.  All terms are squares, so no cancellation occurs and the
+// relative error of every pair addition stays at a few units of 2^-48.  A
+// pair becomes binary64 only at the end of a chunk (one binary64 addition).
+// Squares below binary32's range (|g| < ~1e-23) are lost; they can matter
+// only for a norm below ~1e-19, where the clip coefficient is 1.
 
-// Sum of squares beyond binary64 accuracy, without binary64 multiplies: each
-// square is split exactly into p + e (p = fl(g*g), e = fma(g, g, -p)); the
-// p of a unit are added with Knuth's TwoSum so their rounding errors are kept
-// too; the unit's (hi, lo) pair then enters a binary64 accumulator.
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_add(FF a, FF b)
+{
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float v = __fsub_rn(s, a.hi);
+    float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, v)), __fsub_rn(b.hi, v));
+    e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s, e);
+    return FF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
 struct SumSq {
-    double acc = 0.0;
+    FF acc{0.0f, 0.0f};
 
     __device__ __forceinline__ void add8(const float g[8])
     {
@@ -512,55 +534,163 @@ struct SumSq {
             hi = s;
             lo = __fadd_rn(lo, __fadd_rn(err, e));
         }
-        acc = __dadd_rn(acc, __dadd_rn((double)hi, (double)lo));
+        acc = ff_add(acc, FF{hi, lo});
     }
 };
 
-// Deterministic CTA sum of one double per thread: a fixed butterfly inside
-// each warp, then warp 0 adds the warp sums in warp order.  Valid in thread 0.
-__device__ __forceinline__ double block_sum(double x)
-{
-    __shared__ double warp_sums[kThreads / 32];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0)
-        warp_sums[warp] = x;
-    __syncthreads();
-    double total = 0.0;
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w)
-            total = __dadd_rn(total, warp_sums[w]);
-    }
-    return total;
-}
-
-// Sum of n per-CTA partials in a fixed order, the result valid in every lane
-// of the calling (whole) warp: lane l adds p[l], p[l + 32], p[l + 64] ... in
-// index order from +0 (the loads are issued eight at a time; the order of
-// the additions does not change), then a fixed butterfly combines the lanes.
-__device__ __forceinline__ double warp_fixed_sum(const double *p, int n)
+// Sum of n doubles in a fixed order, the result valid in every lane of the
+// calling (whole) warp: lane l adds p[l], p[l + 32], p[l + 64] ... in index
+// order from +0 (the loads are issued eight at a time; the order of the
+// additions does not change), then a fixed butterfly combines the lanes.
+// The values may have been written by other CTAs of the running kernel, so
+// they are read from L2 (ld.global.cg), past this SM's L1.
+__device__ __forceinline__ double warp_fixed_sum(const double *p, int64_t n)
 {
     const int lane = threadIdx.x & 31;
     double x = 0.0;
-    int i = lane;
+    int64_t i = lane;
     for (; i + 7 * 32 < n; i += 8 * 32) {
         double y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            y[j] = p[i + 32 * j];
+            y[j] = __ldcg(p + i + 32 * j);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             x = __dadd_rn(x, y[j]);
     }
     for (; i < n; i += 32)
-        x = __dadd_rn(x, p[i]);
+        x = __dadd_rn(x, __ldcg(p + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
     return x;
+}
+
+// ------------------------------------------------------------------ the norm's tree
+//
+// Chunks, superchunks, ranks (see NormPlan in internal.h).  A launch walks its
+// chunks with a grid stride; a whole CTA sums one chunk.  Every-rank launches
+// take the chunks bucket by bucket (rank by rank inside a bucket), i.e. in
+// flat order; one rank's view takes them in that rank's element order.
+
+// Where a chunk lies and where its sum goes.
+struct ChunkLoc {
+    int64_t r;        // rank, relative to the launch (0 for one rank's view)
+    int64_t bl;       // bucket, relative to the launch
+    int64_t u0, n_u;  // its units within the rank's slice of that bucket
+    int64_t ci;       // its slot in the chunk sums
+    int64_t sc0;      // slot of its superchunk's first chunk
+    int64_t sci;      // its superchunk's slot
+    int32_t sc_size;  // chunks in that superchunk
+};
+
+__device__ __forceinline__ ChunkLoc locate_chunk(const NormPlan &np, int64_t pi)
+{
+    ChunkLoc L;
+    const bool has_last = np.b0 + np.nbl == np.nb;
+    const int64_t per_bucket = (int64_t)np.ranks * np.cps;
+    const int64_t n_full = (np.nbl - (has_last ? 1 : 0)) * per_bucket;
+    int64_t c, ub, k;
+    if (pi < n_full) {
+        L.bl = pi / per_bucket;
+        const int64_t rem = pi - L.bl * per_bucket;
+        L.r = rem / np.cps;
+        c = rem - L.r * np.cps;
+        ub = np.slice_units;
+        k = (np.b0 + L.bl) * np.cps + c;
+    } else {
+        const int64_t rem = pi - n_full;
+        L.r = rem / np.cps_last;
+        c = rem - L.r * np.cps_last;
+        L.bl = np.nbl - 1;
+        ub = np.last_slice_units;
+        k = (np.nb - 1) * np.cps + c;
+    }
+    L.u0 = c * np.cu;
+    L.n_u = ub - L.u0 < np.cu ? ub - L.u0 : np.cu;
+    L.ci = L.r * np.cpr + k;
+    const int64_t s = k / kNormSuper;
+    L.sci = L.r * np.spr + s;
+    L.sc0 = L.r * np.cpr + s * kNormSuper;
+    const int64_t left = np.cpr - s * kNormSuper;
+    L.sc_size = (int32_t)(left < kNormSuper ? left : kNormSuper);
+    return L;
+}
+
+// Shared state of the tree inside one CTA.
+struct NormShared {
+    FF warp_sum[2][kThreads / 32];  // double-buffered by chunk parity
+    int final_pending;              // this CTA finished the step's last superchunk
+};
+
+// The end of one chunk, called by every thread of the CTA with its own sum:
+// a fixed butterfly inside each warp, the warp sums in warp order, the chunk
+// sum stored; the CTA that brings a superchunk's count to its size sums the
+// superchunk (warp 0, fixed lane order) and counts it as done; the one that
+// completes the last superchunk is marked to finish the tree (norm_finish).
+// Counters return to zero once their superchunk is done.
+__device__ __forceinline__ void norm_chunk_done(const NormPlan &np, const ChunkLoc &L, FF x,
+                                                int parity, NormShared &sh)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const FF y{__shfl_xor_sync(0xFFFFFFFFu, x.hi, o), __shfl_xor_sync(0xFFFFFFFFu, x.lo, o)};
+        x = ff_add(x, y);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0)
+        sh.warp_sum[parity][warp] = x;
+    __syncthreads();
+    if (warp != 0)
+        return;
+    int complete = 0;
+    if (lane == 0) {
+        FF t = sh.warp_sum[parity][0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            t = ff_add(t, sh.warp_sum[parity][w]);
+        np.partials[L.ci] = __dadd_rn((double)t.hi, (double)t.lo);
+        __threadfence();
+        complete = atomicAdd(&np.sc_count[L.sci], 1u) == (uint32_t)(L.sc_size - 1);
+    }
+    complete = __shfl_sync(0xFFFFFFFFu, complete, 0);
+    if (!complete)
+        return;
+    __threadfence();
+    const double s = warp_fixed_sum(np.partials + L.sc0, L.sc_size);
+    if (lane == 0) {
+        np.sc_partials[L.sci] = s;
+        np.sc_count[L.sci] = 0u;
+        __threadfence();
+        if (atomicAdd(np.done, 1u) == (uint32_t)((int64_t)np.ranks * np.spr - 1))
+            sh.final_pending = 1;
+    }
+}
+
+// After a CTA's last chunk (every thread, after a barrier): if this CTA
+// finished the step's last superchunk, sum each rank's superchunks (warp w
+// takes ranks w, w + 8, ...), add the ranks in ascending order from +0, write
+// the total and reset the step's superchunk count.
+__device__ __forceinline__ void norm_finish(const NormPlan &np, NormShared &sh)
+{
+    __shared__ double rank_sum[ZERO_MAX_WORLD];
+    if (!sh.final_pending)
+        return;
+    __threadfence();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r < np.ranks; r += kThreads / 32) {
+        const double s = warp_fixed_sum(np.sc_partials + (int64_t)r * np.spr, np.spr);
+        if (lane == 0)
+            rank_sum[r] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double total = 0.0;
+        for (int r = 0; r < np.ranks; ++r)
+            total = __dadd_rn(total, rank_sum[r]);
+        *np.total = total;
+        *np.done = 0u;
+    }
 }
 
 // Report a non-finite gradient of this warp once.

@@ -9,13 +9,16 @@
 // share of the work, so a second, partial wave would only add a tail).
 //   FUSED      (a2)-(a7) in one pass: reduce, unscale, flag, Adam from slot
 //              cur into slot 1 - cur, cast into the parameter buffer.
-//   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, per-CTA
-//              sums of squares, optionally keep g in a staging buffer.
+//   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, the
+//              sum of squares over the norm's fixed tree (internal.h: chunks
+//              of the layout, not of the grid; the launch that completes the
+//              tree writes the total to the workspace), optionally keep g in
+//              a staging buffer.
 //   PASS2_*    (a5 clip)-(a7) of a clipped step, skipped when pass 1 flagged
-//              an overflow; every CTA first reduces pass 1's per-CTA sums of
-//              squares in one fixed order; g is reduced again or read from
-//              the stage.  It walks the units backwards, starting on the
-//              first pass's last units, whose data pass 1 left in L2.
+//              an overflow; it reads the total pass 1 formed; g is reduced
+//              again or read from the stage.  It walks the units backwards,
+//              starting on the first pass's last units, whose data pass 1
+//              left in L2.
 //   RS         (a2) alone: the reduced fp32 gradient.
 //   RS_ACC     (a2) into an fp32 accumulator (gradient accumulation).
 //   ACC_*      the step with the gradient read from an fp32 accumulator (the
@@ -25,6 +28,7 @@
 // the CTA that finishes last commits or skips the step (a8).  Gradient
 // buffers may be device memory or page-locked host memory, which these
 // kernels load over the host link.
+#include <atomic>
 #include <cstdlib>
 
 #include "kernels.cuh"
@@ -72,8 +76,8 @@ struct StepParams {
     float *wo0, *wo1, *mo0, *mo1, *vo0, *vo1;   // ping-pong slots (writes)
     uint16_t *par0, *par1;                      // parameter buffer slots
     float *stage;      // PASS1 output / PASS2_STAGED input / RS output / accumulator
-    double *partials;  // PASS1: one per CTA; second passes reduce them
-    int32_t n_partials;  // second passes: CTAs of the first pass
+    NormPlan norm;     // first passes: the chunks of the norm's tree this launch forms
+    const double *norm_total;  // second passes: the sum of squares the first pass formed
     int32_t add;       // RS_ACC: add to the accumulator (else overwrite it)
     // Clipped steps: the first pass marks what it reads or writes for units
     // u >= keep_from evict-last in L2 (the stage it writes, else the
@@ -89,6 +93,40 @@ struct StepParams {
     FinCfg fin;
 };
 
+// A first pass's walk over its chunks of the norm's tree: each chunk's units
+// go through `unit` (which adds their squares to ss), then the chunk's sum
+// enters the tree; the CTA that completes the tree finishes it.
+template <bool ALL, class UnitFn>
+__device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, SumSq &ss,
+                                          UnitFn &unit)
+{
+    __shared__ NormShared nsh;
+    if (threadIdx.x == 0)
+        nsh.final_pending = 0;
+    __syncthreads();
+    int parity = 0;
+    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x, parity ^= 1) {
+        const ChunkLoc L = locate_chunk(np, pi);
+        int64_t ubase;  // the launch's unit index of the chunk's first unit
+        if constexpr (ALL) {
+            int64_t flat;
+            if (vw.bucket == 0)
+                flat = L.r * vw.part;
+            else
+                flat = L.bl * vw.bucket + L.r * (L.bl == np.nbl - 1 ? vw.last_slice : vw.slice);
+            ubase = flat / kUnit + L.u0;
+        } else {
+            ubase = L.bl * vw.slice_units + L.u0;
+        }
+        ss.acc = FF{0.0f, 0.0f};
+        for (int64_t k = threadIdx.x; k < L.n_u; k += kThreads)
+            unit(ubase + k);
+        norm_chunk_done(np, L, ss.acc, parity, nsh);
+    }
+    __syncthreads();
+    norm_finish(np, nsh);
+}
+
 // The body of the streaming kernels (the __global__ wrappers below differ
 // only in their launch bounds).
 template <int DT, int W, int MAXW, int MODE, bool ALL, bool HOST_STATE>
@@ -102,19 +140,15 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     if constexpr (!reduces_only(MODE)) {
         if constexpr (second_pass(MODE)) {
-            // The global sum of squares, reduced by every CTA from the first
-            // pass's per-CTA partials in one fixed order (all CTAs get the
-            // same bits); CTA 0 publishes it in the state.
-            if (threadIdx.x < 32) {
-                const double x = warp_fixed_sum(p.partials, p.n_partials);
-                if (threadIdx.x == 0) {
-                    const double total = __dadd_rn(0.0, x);
-                    compute_scalars(p.cfg, p.state, total, sh);
-                    sh_cur = p.state->cur;
-                    if (blockIdx.x == 0 && !sh.skip) {
-                        p.state->sumsq = total;
-                        p.state->clip_coef = sh.coef;
-                    }
+            // The global sum of squares the first pass formed; CTA 0
+            // publishes it in the state when the step is not skipped.
+            if (threadIdx.x == 0) {
+                const double total = __ldcg(p.norm_total);
+                compute_scalars(p.cfg, p.state, total, sh);
+                sh_cur = p.state->cur;
+                if (blockIdx.x == 0 && !sh.skip) {
+                    p.state->sumsq = total;
+                    p.state->clip_coef = sh.coef;
                 }
             }
         } else if (threadIdx.x == 0) {
@@ -242,7 +276,9 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     };
 
     const int64_t base = (int64_t)blockIdx.x * kThreads;
-    if constexpr (second_pass(MODE)) {
+    if constexpr (sums_squares(MODE)) {
+        norm_loop<ALL>(p.norm, vw, ss, unit);
+    } else if constexpr (second_pass(MODE)) {
         // Backwards over the grid-stride sequence: the units the first pass
         // reached last come first, while their lines can still be in L2.
         if (work && base < vw.units) {
@@ -267,11 +303,6 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     }
     if constexpr (flags_overflow(MODE))
         flag_nonfinite(bad, &p.state->found_inf);
-    if constexpr (sums_squares(MODE)) {
-        const double tot = block_sum(ss.acc);
-        if (threadIdx.x == 0)
-            p.partials[blockIdx.x] = tot;
-    }
     if constexpr (ends_step(MODE)) {
         if (p.end_step)
             arrive_and_end_step(p.fin, p.state);
@@ -314,7 +345,8 @@ int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
         kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true>
                                 : step_kernel<DT, W, MAXW, MODE, false>;
     const int target = target_ctas(reinterpret_cast<const void *>(kern));
-    const int64_t want = (p.view.units + kThreads - 1) / kThreads;
+    const int64_t want = sums_squares(MODE) ? p.norm.launch_chunks
+                                            : (p.view.units + kThreads - 1) / kThreads;
     const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
     if (gx_out)
         *gx_out = (int)gx;
@@ -384,20 +416,21 @@ int dispatch(const StepParams<MAXW> &p, zero_dtype dt, int mode, cudaStream_t s,
 
 // Everything a pass needs besides the per-mode pointers.
 struct PassArgs {
-    const void *const *grads;
-    int grads_are_slices;
-    zero_dtype dtype;
-    const zero_layout *lay;
-    int rank;
-    const zero_adam_cfg *cfg;
-    zero_step_state *state;
-    float *const *master, *const *m, *const *v;
-    void *const *params;
-    float *stage;
-    double *partials;
-    int add;
-    bool host_state = false;  // master/m/v in pinned host memory (one-pass step only)
-    int n_partials = 0;       // second passes: CTAs of the first pass
+    const void *const *grads = nullptr;
+    int grads_are_slices = 0;
+    zero_dtype dtype = ZERO_F16;
+    const zero_layout *lay = nullptr;  // the launch's (sub-)layout; buffers start at its origin
+    int rank = -1;
+    const zero_adam_cfg *cfg = nullptr;
+    zero_step_state *state = nullptr;
+    float *const *master = nullptr, *const *m = nullptr, *const *v = nullptr;
+    void *const *params = nullptr;
+    float *stage = nullptr;
+    int add = 0;
+    bool host_state = false;       // master/m/v in pinned host memory (one-pass step only)
+    bool grads_on_device = true;   // every gradient buffer is device memory
+    NormPlan norm{};               // first passes: their chunks of the norm's tree
+    const double *norm_total = nullptr;  // second passes: the first pass's total
     int64_t keep_from = INT64_MAX;  // clipped steps: see StepParams
     bool discard = false;
     bool end_step = false;    // the launch is the step's last: it ends the step
@@ -456,8 +489,8 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
         p.par1 = static_cast<uint16_t *>(a.params[1]);
     }
     p.stage = a.stage;
-    p.partials = a.partials;
-    p.n_partials = a.n_partials;
+    p.norm = a.norm;
+    p.norm_total = a.norm_total;
     p.add = a.add;
     p.keep_from = a.keep_from < v.units ? a.keep_from : v.units;
     p.discard = a.discard && p.keep_from < v.units ? 1 : 0;
@@ -495,28 +528,63 @@ int check_grads(const void *const *grads, int grads_are_slices, zero_dtype dtype
     return ZERO_OK;
 }
 
-// Where a buffer lives: 1 pinned host memory, 0 device memory, -1 neither
-// (pageable host memory or an unknown pointer).
-int residence(const void *p)
+// Where a buffer lives: 1 page-locked host memory, 0 memory of device `dev`
+// (or managed memory), -1 anything else (pageable host memory, an unknown
+// pointer, another device's memory).
+int residence(const void *p, int dev)
 {
     cudaPointerAttributes attr;
     if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return -1;
     }
-    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
+    if (attr.type == cudaMemoryTypeManaged)
         return 0;
+    if (attr.type == cudaMemoryTypeDevice)
+        return attr.device == dev ? 0 : -1;
     return attr.type == cudaMemoryTypeHost ? 1 : -1;
+}
+
+int current_device(int *dev)
+{
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cuda_error(e);
+    }
+    return ZERO_OK;
+}
+
+// Every gradient buffer must be memory the kernels can load: device memory
+// of the current device or page-locked host memory.  One query per buffer;
+// *all_device tells whether the bulk-copy (staged) kernel may take them.
+int check_grad_residence(const void *const *grads, int world, bool *all_device)
+{
+    int dev = 0, rc = current_device(&dev);
+    if (rc)
+        return rc;
+    bool on_device = true;
+    for (int q = 0; q < world; ++q) {
+        const int r = residence(grads[q], dev);
+        if (r < 0)
+            return ZERO_EINVAL;
+        on_device = on_device && r == 0;
+    }
+    *all_device = on_device;
+    return ZERO_OK;
 }
 
 // 1 when all six master/m/v slots are pinned host memory (offload), 0 when
 // all are device memory, ZERO_EINVAL otherwise.
 int state_residence(float *const master[2], float *const m[2], float *const v[2])
 {
+    int dev = 0, rc = current_device(&dev);
+    if (rc)
+        return rc;
     const void *ptrs[6] = {master[0], master[1], m[0], m[1], v[0], v[1]};
-    int first = residence(ptrs[0]);
+    const int first = residence(ptrs[0], dev);
     for (int i = 1; i < 6; ++i)
-        if (residence(ptrs[i]) != first)
+        if (ptrs[i] != ptrs[i - 1] && residence(ptrs[i], dev) != first)
             return ZERO_EINVAL;
     return first < 0 ? ZERO_EINVAL : first;
 }
@@ -544,6 +612,18 @@ int check_pingpong(const zero_layout *layout, const zero_adam_cfg *cfg, float *c
     return ZERO_OK;
 }
 
+// The workspace of a step on `layout`.
+int check_ws(const zero_layout *layout, const void *ws, size_t ws_bytes)
+{
+    if (!ws)
+        return ZERO_EINVAL;
+    if (!aligned16(ws))
+        return ZERO_EALIGN;
+    if (ws_bytes < zero_workspace_bytes(layout))
+        return ZERO_ESPACE;
+    return ZERO_OK;
+}
+
 // check_pingpong, plus the stage and the workspace.
 int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *const master[2],
                 float *const m[2], float *const v[2], void *const params[2], const float *stage,
@@ -557,62 +637,102 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
         return rc;
     if (stage && !stage_allowed)
         return ZERO_EINVAL;
-    if ((stage && !aligned32(stage)) || !aligned16(ws))
+    if (stage && !aligned32(stage))
         return ZERO_EALIGN;
-    if (ws_bytes < zero_workspace_bytes(layout->world))
-        return ZERO_ESPACE;
-    return ZERO_OK;
+    return check_ws(layout, ws, ws_bytes);
+}
+
+// The norm's tree for launches over buckets [b0, b0 + nbl) of `L` (the whole
+// layout), in workspace ws.
+NormPlan layout_plan(const zero_layout &L, int rank, int64_t b0, int64_t nbl, void *ws)
+{
+    const bool bucketed = L.bucket_numel > 0;
+    const int64_t nb = bucketed ? L.num_buckets : 1;
+    const int64_t su = (bucketed ? L.slice_numel : L.owned_numel) / kUnit;
+    const int64_t lsu = L.last_slice_numel / kUnit;
+    return norm_plan(norm_geometry(su, lsu, nb), su, lsu, nb, b0, nbl,
+                     rank < 0 ? L.world : 1, ws, nullptr);
+}
+
+// Polls of the staged kernel's stage waits; a test may lower the limit with
+// ZERO_TEST_STAGED_WAIT_LIMIT (read once per process), and then also makes
+// every wait run out (see staged.cuh).
+long long staged_test_wait_limit()
+{
+    static const long long n = [] {
+        const char *t = std::getenv("ZERO_TEST_STAGED_WAIT_LIMIT");
+        const long long v = t ? std::atoll(t) : 0;
+        return v > 0 ? v : 0LL;
+    }();
+    return n;
+}
+
+// Resident CTAs per SM of the staged kernel on device `dev` after raising its
+// dynamic shared-memory limit there (the attribute belongs to the device):
+// found once per device; 0 when the kernel cannot run there.
+constexpr int kStagedDevices = 64;
+
+template <int DT, int W>
+int staged_resident(int dev)
+{
+    static std::atomic<int> cache[kStagedDevices];  // 0 unknown, -1 unusable, > 0 CTAs per SM
+    if (dev >= 0 && dev < kStagedDevices) {
+        const int c = cache[dev].load(std::memory_order_acquire);
+        if (c != 0)
+            return c > 0 ? c : 0;
+    }
+    int occ = 0;
+    if (cudaFuncSetAttribute(staged_fused_kernel<DT, W>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStagedSmemBudget) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, staged_fused_kernel<DT, W>,
+                                                      kStagedThreads, kStagedSmemBudget) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        occ = 0;
+    }
+    if (dev >= 0 && dev < kStagedDevices)
+        cache[dev].store(occ > 0 ? occ : -1, std::memory_order_release);
+    return occ > 0 ? occ : 0;
 }
 
 // The staged one-pass step (staged.cuh), when it applies: every rank at once,
-// fp32 reduction, device-resident state, N_d = 16.  Returns 1 when it does not
-// apply (the caller then uses the register path).
+// fp32 reduction, device-resident state and gradients, N_d = 16.  Returns 1
+// when it does not apply or cannot be launched (the caller then uses the
+// register path).
 template <int DT, int W>
 int launch_staged_w(const StagedParams &p, cudaStream_t stream)
 {
-    static const int resident = [] {
-        if (cudaFuncSetAttribute(staged_fused_kernel<DT, W>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kStagedSmemBudget) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return 0;
-        }
-        int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, staged_fused_kernel<DT, W>,
-                                                          kStagedThreads, kStagedSmemBudget) !=
-            cudaSuccess) {
-            (void)cudaGetLastError();
-            return 0;
-        }
-        return occ;
-    }();
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    const int resident = staged_resident<DT, W>(dev);
     if (resident < 1)
         return 1;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 1;
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
-    const int64_t want = (int64_t)sms * resident;
+    int64_t want = (int64_t)device_sms() * resident;
+    const int cap = test_grid_cap();
+    if (cap > 0 && want > cap)
+        want = cap;
     const unsigned grid = (unsigned)(tiles < want ? tiles : want);
     staged_fused_kernel<DT, W>
         <<<grid, kStagedThreads, p.stages * staged_stage_bytes(W), stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+    if (cudaGetLastError() != cudaSuccess)
+        return 1;  // not launched: the register kernel takes the step
+    return ZERO_OK;
 }
 
 int launch_staged(const PassArgs &a, cudaStream_t stream)
 {
     const zero_layout &L = *a.lay;
     const int stages = staged_stages(L.world);
-    if (a.rank >= 0 || a.host_state || half_reduce(a.dtype) || L.world != kStagedWorld ||
-        stages < 2 || L.padded_numel <= 0)
-        return 1;
     // The bulk copies serve gradients in device memory; gradients in
     // page-locked host memory are loaded by the register kernel.
-    for (int q = 0; q < L.world; ++q)
-        if (residence(a.grads[q]) != 0)
-            return 1;
+    if (a.rank >= 0 || a.host_state || !a.grads_on_device || half_reduce(a.dtype) ||
+        L.world != kStagedWorld || stages < 2 || L.padded_numel <= 0)
+        return 1;
     StagedParams p{};
     for (int q = 0; q < L.world; ++q)
         p.g[q] = static_cast<const uint16_t *>(a.grads[q]);
@@ -634,12 +754,9 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
     p.fin = fin_cfg(c);
     p.spin_limit = kStageSpinLimit;
     p.tx_extra = 0;
-    if (const char *t = std::getenv("ZERO_TEST_STAGED_WAIT_LIMIT")) {  // tests only
-        const long long n = std::atoll(t);
-        if (n > 0) {
-            p.spin_limit = n;
-            p.tx_extra = 16;
-        }
+    if (const long long n = staged_test_wait_limit()) {  // tests only
+        p.spin_limit = n;
+        p.tx_extra = 16;
     }
     return is_bf16(a.dtype) ? launch_staged_w<ZERO_BF16, kStagedWorld>(p, stream)
                             : launch_staged_w<ZERO_F16, kStagedWorld>(p, stream);
@@ -653,20 +770,20 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
 #endif
 constexpr int64_t kKeepBytes = (int64_t)ZS_KEEP_MB << 20;
 
-// One step (one or two passes) in the given modes.  With commit the step's
+// One whole step (one or two passes) in the given modes on a.lay.  The step's
 // last launch also ends the step (a8: its last CTA commits or skips); an empty
 // vector runs no pass and ends the step with the one-thread kernel.  A clipped
-// step's second pass reduces the first pass's per-CTA sums of squares itself
-// (there is no separate norm kernel).
-int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStream_t stream,
-             bool commit = true)
+// step's first pass forms the norm's tree in ws and the second pass reads its
+// total.
+int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, void *ws,
+             cudaStream_t stream)
 {
     int rc, gx = 1;
     const zero_layout &L = *a.lay;
     if (L.padded_numel == 0)
-        return commit ? launch_finalize(a.cfg, a.state, 1, stream) : ZERO_OK;
+        return launch_finalize(a.cfg, a.state, 1, stream);
     if (!clip) {
-        a.end_step = commit;
+        a.end_step = true;
         rc = one_pass == M_FUSED ? launch_staged(a, stream) : 1;
         if (rc == 1)
             rc = run(a, one_pass, stream, &gx);
@@ -680,12 +797,69 @@ int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, cudaStr
     a.keep_from = from < units ? from : units;
     a.discard = a.stage && pass2 == M_PASS2_STAGED &&
                 (reinterpret_cast<uintptr_t>(a.stage) & 127u) == 0;
+    a.norm = layout_plan(L, a.rank, 0, L.bucket_numel ? L.num_buckets : 1, ws);
+    a.norm_total = norm_total_slot(ws);
     a.end_step = false;
     if ((rc = run(a, pass1, stream, &gx)))
         return rc;
-    a.n_partials = gx;
-    a.end_step = commit;
+    a.end_step = true;
     return run(a, pass2, stream, &gx);
+}
+
+// A range of buckets [first, first + n) of L as a layout of its own, with the
+// offsets of its first element in flat buffers, in rank-order buffers and in
+// the gradient buffers.
+struct Range {
+    zero_layout lay;
+    int64_t flat_off, owned_off, state_off, grad_off;
+};
+
+Range bucket_range(const zero_layout &L, int rank, int grads_are_slices, int64_t first, int64_t n)
+{
+    Range R{L, 0, 0, 0, 0};
+    if (L.bucket_numel > 0) {
+        zero_layout &S = R.lay;
+        const int64_t end = first + n;
+        S.num_buckets = n;
+        S.last_slice_numel = end == L.num_buckets ? L.last_slice_numel : L.slice_numel;
+        S.owned_numel = (n - 1) * L.slice_numel + S.last_slice_numel;
+        S.padded_numel = S.owned_numel * L.world;
+        S.numel = S.flat_numel = S.padded_numel;
+        R.flat_off = first * L.bucket_numel;
+        R.owned_off = first * L.slice_numel;
+    }
+    R.state_off = rank < 0 ? R.flat_off : R.owned_off;
+    R.grad_off = grads_are_slices ? R.owned_off : R.flat_off;
+    return R;
+}
+
+// Checks of a bucket range.
+int check_range(const zero_layout &L, int64_t first, int64_t n)
+{
+    if (first < 0 || n < 0 || first > L.num_buckets - n)
+        return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+// Buffers offset to a range's first element.
+struct RangeBuffers {
+    const void *g[ZERO_MAX_WORLD];
+    float *w[2], *m[2], *v[2];
+    void *par[2];
+};
+
+void offset_buffers(const Range &R, const void *const *grads, int world, float *const master[2],
+                    float *const m[2], float *const v[2], void *const params[2], RangeBuffers &B)
+{
+    if (grads)
+        for (int q = 0; q < world; ++q)
+            B.g[q] = static_cast<const uint16_t *>(grads[q]) + R.grad_off;
+    for (int s = 0; s < 2; ++s) {
+        B.w[s] = master ? master[s] + R.state_off : nullptr;
+        B.m[s] = m ? m[s] + R.state_off : nullptr;
+        B.v[s] = v ? v[s] + R.state_off : nullptr;
+        B.par[s] = params ? static_cast<uint16_t *>(params[s]) + R.flat_off : nullptr;
+    }
 }
 
 }  // namespace zs
@@ -705,8 +879,16 @@ extern "C" int zero_reduce_scatter_sum(const void *const *grads, int grads_are_s
         return ZERO_EALIGN;
     if (layout->padded_numel == 0)
         return ZERO_OK;
-    PassArgs a{grads, grads_are_slices, dtype, layout, rank, nullptr, nullptr,
-               nullptr, nullptr, nullptr, nullptr, g_out, nullptr, 0};
+    bool on_device;
+    if ((rc = check_grad_residence(grads, layout->world, &on_device)))
+        return rc;
+    PassArgs a;
+    a.grads = grads;
+    a.grads_are_slices = grads_are_slices;
+    a.dtype = dtype;
+    a.lay = layout;
+    a.rank = rank;
+    a.stage = g_out;
     int gx;
     return run(a, M_RS, stream, &gx);
 }
@@ -724,8 +906,17 @@ extern "C" int zero_reduce_scatter_accumulate(const void *const *grads, int grad
         return ZERO_EALIGN;
     if (layout->padded_numel == 0)
         return ZERO_OK;
-    PassArgs a{grads, grads_are_slices, dtype, layout, rank, nullptr, nullptr,
-               nullptr, nullptr, nullptr, nullptr, acc, nullptr, add ? 1 : 0};
+    bool on_device;
+    if ((rc = check_grad_residence(grads, layout->world, &on_device)))
+        return rc;
+    PassArgs a;
+    a.grads = grads;
+    a.grads_are_slices = grads_are_slices;
+    a.dtype = dtype;
+    a.lay = layout;
+    a.rank = rank;
+    a.stage = acc;
+    a.add = add ? 1 : 0;
     int gx;
     return run(a, M_RS_ACC, stream, &gx);
 }
@@ -746,16 +937,28 @@ extern "C" int zero_step_fused(const void *const *grads, int grads_are_slices, z
     if ((rc = check_slots(layout, cfg, master, m, v, params, g_stage, clip, state_dev, ws,
                           ws_bytes)))
         return rc;
-    double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
-    PassArgs a{grads, grads_are_slices, dtype, layout, rank, cfg, state_dev,
-               master, m, v, params, g_stage, partials, 0};
+    PassArgs a;
+    a.grads = grads;
+    a.grads_are_slices = grads_are_slices;
+    a.dtype = dtype;
+    a.lay = layout;
+    a.rank = rank;
+    a.cfg = cfg;
+    a.state = state_dev;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.params = params;
+    a.stage = g_stage;
     if (layout->padded_numel > 0) {
+        if ((rc = check_grad_residence(grads, layout->world, &a.grads_on_device)))
+            return rc;
         const int where = state_residence(master, m, v);
         if (where < 0 || (where == 1 && clip))
             return ZERO_EINVAL;  // mixed residence, or offloaded state with the clip
         a.host_state = where == 1;
     }
-    return run_step(a, clip, M_FUSED, M_PASS1, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE,
+    return run_step(a, clip, M_FUSED, M_PASS1, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE, ws,
                     stream);
 }
 
@@ -780,10 +983,18 @@ extern "C" int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
     if ((rc = check_slots(layout, cfg, master, m, v, params, nullptr, false, state_dev, ws,
                           ws_bytes)))
         return rc;
-    double *partials = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsHeader);
-    PassArgs a{nullptr, 0, dtype, layout, rank, cfg, state_dev,
-               master, m, v, params, const_cast<float *>(acc), partials, 0};
-    return run_step(a, clip, M_ACC_FUSED, M_ACC_PASS1, M_ACC_PASS2, stream);
+    PassArgs a;
+    a.dtype = dtype;
+    a.lay = layout;
+    a.rank = rank;
+    a.cfg = cfg;
+    a.state = state_dev;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.params = params;
+    a.stage = const_cast<float *>(acc);
+    return run_step(a, clip, M_ACC_FUSED, M_ACC_PASS1, M_ACC_PASS2, ws, stream);
 }
 
 extern "C" int zero_step_fused_buckets(const void *const *grads, int grads_are_slices,
@@ -800,8 +1011,7 @@ extern "C" int zero_step_fused_buckets(const void *const *grads, int grads_are_s
     if ((rc = check_cfg(cfg)))
         return rc;
     const zero_layout &L = *layout;
-    if (cfg->max_grad_norm > 0.0 || first_bucket < 0 || n_buckets < 0 ||
-        first_bucket > L.num_buckets - n_buckets)
+    if (cfg->max_grad_norm > 0.0 || check_range(L, first_bucket, n_buckets))
         return ZERO_EINVAL;
     if ((rc = check_pingpong(layout, cfg, master, m, v, params, state_dev)))
         return rc;
@@ -810,33 +1020,137 @@ extern "C" int zero_step_fused_buckets(const void *const *grads, int grads_are_s
     // The buckets of the range as a layout of their own; the buffers are
     // offset to the range's first element.  Each bucket's rank slices lie
     // inside it, so the range is a self-contained bucketed vector.
-    zero_layout S = L;
-    int64_t flat_off = 0, owned_off = 0;
-    if (L.bucket_numel > 0) {
-        const int64_t end = first_bucket + n_buckets;
-        S.num_buckets = n_buckets;
-        S.last_slice_numel = end == L.num_buckets ? L.last_slice_numel : L.slice_numel;
-        S.owned_numel = (n_buckets - 1) * L.slice_numel + S.last_slice_numel;
-        S.padded_numel = S.owned_numel * L.world;
-        S.numel = S.flat_numel = S.padded_numel;
-        flat_off = first_bucket * L.bucket_numel;
-        owned_off = first_bucket * L.slice_numel;
-    }
-    const int64_t state_off = rank < 0 ? flat_off : owned_off;
-    const int64_t grad_off = grads_are_slices ? owned_off : flat_off;
-    const void *g[ZERO_MAX_WORLD];
-    for (int q = 0; q < L.world; ++q)
-        g[q] = static_cast<const uint16_t *>(grads[q]) + grad_off;
-    float *w2[2] = {master[0] + state_off, master[1] + state_off};
-    float *m2[2] = {m[0] + state_off, m[1] + state_off};
-    float *v2[2] = {v[0] + state_off, v[1] + state_off};
-    void *p2[2] = {static_cast<uint16_t *>(params[0]) + flat_off,
-                   static_cast<uint16_t *>(params[1]) + flat_off};
-    PassArgs a{g, grads_are_slices, dtype, &S, rank, cfg, state_dev,
-               w2, m2, v2, p2, nullptr, nullptr, 0};
-    const int where = state_residence(w2, m2, v2);
+    const Range R = bucket_range(L, rank, grads_are_slices, first_bucket, n_buckets);
+    RangeBuffers B;
+    offset_buffers(R, grads, L.world, master, m, v, params, B);
+    PassArgs a;
+    a.grads = B.g;
+    a.grads_are_slices = grads_are_slices;
+    a.dtype = dtype;
+    a.lay = &R.lay;
+    a.rank = rank;
+    a.cfg = cfg;
+    a.state = state_dev;
+    a.master = B.w;
+    a.m = B.m;
+    a.v = B.v;
+    a.params = B.par;
+    if ((rc = check_grad_residence(B.g, L.world, &a.grads_on_device)))
+        return rc;
+    const int where = state_residence(B.w, B.m, B.v);
     if (where < 0)
         return ZERO_EINVAL;  // mixed residence
     a.host_state = where == 1;
-    return run_step(a, false, M_FUSED, M_PASS1, M_PASS2_RECOMPUTE, stream, false);
+    rc = launch_staged(a, stream);
+    if (rc == 1) {
+        int gx;
+        rc = run(a, M_FUSED, stream, &gx);
+    }
+    return rc;
+}
+
+// Checks shared by the two passes of a clipped step on a range of buckets.
+static int check_range_pass(const void *const *grads, int grads_are_slices, zero_dtype dtype,
+                            const zero_layout *layout, int rank, int64_t first_bucket,
+                            int64_t n_buckets, const zero_adam_cfg *cfg,
+                            const zero_step_state *state_dev, const void *ws, size_t ws_bytes)
+{
+    int rc = grads ? check_grads(grads, grads_are_slices, dtype, layout, rank)
+                   : check_layout(layout);
+    if (rc)
+        return rc;
+    if (dtype < ZERO_F16 || dtype > ZERO_BF16_HALF_REDUCE || rank < -1 ||
+        rank >= layout->world || (grads_are_slices && rank < 0))
+        return ZERO_EINVAL;
+    if ((rc = check_cfg(cfg)))
+        return rc;
+    if (!(cfg->max_grad_norm > 0.0) || !state_dev ||
+        check_range(*layout, first_bucket, n_buckets))
+        return ZERO_EINVAL;
+    if (reinterpret_cast<uintptr_t>(state_dev) & 7u)
+        return ZERO_EALIGN;
+    return check_ws(layout, ws, ws_bytes);
+}
+
+extern "C" int zero_step_buckets_pass1(const void *const *grads, int grads_are_slices,
+                                       zero_dtype dtype, const zero_layout *layout, int rank,
+                                       int64_t first_bucket, int64_t n_buckets, float *g_stage,
+                                       const zero_adam_cfg *cfg, zero_step_state *state_dev,
+                                       void *ws, size_t ws_bytes, zero_stream_t stream)
+{
+    if (!grads)
+        return ZERO_EINVAL;
+    int rc = check_range_pass(grads, grads_are_slices, dtype, layout, rank, first_bucket,
+                              n_buckets, cfg, state_dev, ws, ws_bytes);
+    if (rc)
+        return rc;
+    if (g_stage && !aligned32(g_stage))
+        return ZERO_EALIGN;
+    const zero_layout &L = *layout;
+    if (n_buckets == 0 || L.padded_numel == 0)
+        return ZERO_OK;
+    const Range R = bucket_range(L, rank, grads_are_slices, first_bucket, n_buckets);
+    RangeBuffers B;
+    offset_buffers(R, grads, L.world, nullptr, nullptr, nullptr, nullptr, B);
+    PassArgs a;
+    a.grads = B.g;
+    a.grads_are_slices = grads_are_slices;
+    a.dtype = dtype;
+    a.lay = &R.lay;
+    a.rank = rank;
+    a.cfg = cfg;
+    a.state = state_dev;
+    a.stage = g_stage ? g_stage + R.state_off : nullptr;
+    if ((rc = check_grad_residence(B.g, L.world, &a.grads_on_device)))
+        return rc;
+    a.norm = layout_plan(L, rank, first_bucket, n_buckets, ws);
+    int gx;
+    return run(a, M_PASS1, stream, &gx);
+}
+
+extern "C" int zero_step_buckets_pass2(const void *const *grads, int grads_are_slices,
+                                       zero_dtype dtype, const zero_layout *layout, int rank,
+                                       int64_t first_bucket, int64_t n_buckets,
+                                       float *const master[2], float *const m[2],
+                                       float *const v[2], void *const params[2],
+                                       const float *g_stage, const zero_adam_cfg *cfg,
+                                       zero_step_state *state_dev, const void *ws,
+                                       size_t ws_bytes, zero_stream_t stream)
+{
+    if (!grads == !g_stage)
+        return ZERO_EINVAL;  // exactly one source of the gradient
+    int rc = check_range_pass(grads, grads_are_slices, dtype, layout, rank, first_bucket,
+                              n_buckets, cfg, state_dev, ws, ws_bytes);
+    if (rc)
+        return rc;
+    if ((rc = check_pingpong(layout, cfg, master, m, v, params, state_dev)))
+        return rc;
+    if (g_stage && !aligned32(g_stage))
+        return ZERO_EALIGN;
+    const zero_layout &L = *layout;
+    if (n_buckets == 0 || L.padded_numel == 0)
+        return ZERO_OK;
+    const Range R = bucket_range(L, rank, grads_are_slices, first_bucket, n_buckets);
+    RangeBuffers B;
+    offset_buffers(R, grads, L.world, master, m, v, params, B);
+    PassArgs a;
+    a.grads = grads ? B.g : nullptr;
+    a.grads_are_slices = grads_are_slices;
+    a.dtype = dtype;
+    a.lay = &R.lay;
+    a.rank = rank;
+    a.cfg = cfg;
+    a.state = state_dev;
+    a.master = B.w;
+    a.m = B.m;
+    a.v = B.v;
+    a.params = B.par;
+    a.stage = g_stage ? const_cast<float *>(g_stage) + R.state_off : nullptr;
+    if (grads && (rc = check_grad_residence(B.g, L.world, &a.grads_on_device)))
+        return rc;
+    if (state_residence(B.w, B.m, B.v) != 0)
+        return ZERO_EINVAL;  // the clipped step keeps its state in device memory
+    a.norm_total = norm_total_slot(const_cast<void *>(ws));
+    int gx;
+    return run(a, g_stage ? M_PASS2_STAGED : M_PASS2_RECOMPUTE, stream, &gx);
 }
