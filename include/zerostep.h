@@ -222,7 +222,9 @@ ZERO_API int zero_state_init(zero_step_state *host_state, float loss_scale);
  * so the sum's bits do not depend on the GPU, the grid, or how the buckets
  * are split into ranges.  It also holds counters: ZERO-FILL THE WORKSPACE
  * ONCE before its first use; every call that runs to completion leaves the
- * counters at zero again.
+ * counters at zero again.  A workspace serves the steps of one layout (every
+ * rank's view of it), or zero_grad_norm: its counters sit where the calls of
+ * that one use expect them.
  */
 ZERO_API size_t zero_workspace_bytes(const zero_layout *layout);
 

@@ -147,3 +147,43 @@ def test_clipped_bucket_ranges_equal_fused_step(name):
         ref.check()
     assert ref.st.skipped == 1 and ref.st.t == wl.steps - 1
     assert ref.st.coef < 1.0  # the clip was active
+
+
+def test_one_norm_workspace_serves_any_sequence_of_lengths():
+    """zero_grad_norm with one workspace over vectors of growing and
+    shrinking length (their trees have different numbers of chunks) gives
+    each vector the bits a fresh workspace gives it."""
+    import synth
+    ws = zs.new_workspace()
+    for n in (37, 300_000_001, 1000, 6_000_005, 300_000_001, 8):
+        g = torch.empty(n, dtype=torch.float32, device="cuda")
+        synth.gpu_fill_f32(synth.key(5, n), 0, g, 1e-2)
+        a = torch.zeros(1, dtype=torch.float64, device="cuda")
+        b = torch.zeros(1, dtype=torch.float64, device="cuda")
+        zs.zero_grad_norm(g, 1.0, a.data_ptr(), ws)
+        zs.zero_grad_norm(g, 1.0, b.data_ptr(), zs.new_workspace())
+        assert _bits(float(a.item())) == _bits(float(b.item())), n
+        del g
+        torch.cuda.empty_cache()
+
+
+def test_one_step_workspace_serves_every_view():
+    """The clipped step's workspace shared by an every-rank group and a
+    one-rank group of the same layout, alternating steps: each gets the bits
+    it gets with a workspace of its own."""
+    wl, kw = NORM_CASES["decoder-nd8-buckets-recompute"]
+    view = wl.replace(rank=3)
+    shared_all, shared_one = Lockstep(wl, **kw), Lockstep(view, **kw)
+    own_all, own_one = Lockstep(wl, **kw), Lockstep(view, **kw)
+    shared_one.z.ws = shared_all.z.ws
+    for s in (1, 2, 3):
+        grads = gen_grads(wl, own_all.lay, s, own_all.st.loss_scale)
+        for ls in (shared_all, shared_one, own_all, own_one):
+            ls.step(grads)
+        torch.cuda.synchronize()
+        for a, b in ((shared_all, own_all), (shared_one, own_one)):
+            assert bytes(a.z.read_state()) == bytes(b.z.read_state()), s
+            for x, y in zip(a.z.current(), b.z.current()):
+                assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), s
+    own_all.check()
+    own_one.check()

@@ -179,9 +179,14 @@ static int launch_norm(const float *g, int64_t n, float inv_scale, double *sumsq
     }
     const int64_t units = (n + kUnit - 1) / kUnit;
     const NormGeom geo = norm_geometry(units, units, 1);
-    if (norm_ws_bytes(1, geo) > ws_bytes)
+    const size_t need = kWsHeader + (kNormChunksPerRank / kNormSuper) * sizeof(uint32_t) +
+                        (size_t)(geo.cpr + geo.spr) * sizeof(double);
+    if (need > ws_bytes)
         return ZERO_ESPACE;
-    const NormPlan np = norm_plan(geo, units, units, 1, 0, 1, 1, ws, sumsq_dev);
+    // the counters of the longest vector's tree, so any sequence of lengths
+    // finds its counters at zero
+    const NormPlan np = norm_plan(geo, units, units, 1, 0, 1, 1,
+                                  kNormChunksPerRank / kNormSuper, ws, sumsq_dev);
     const int target = target_ctas(reinterpret_cast<const void *>(norm_kernel));
     const int gx = (int)(np.launch_chunks < target ? np.launch_chunks : target);
     norm_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, np);

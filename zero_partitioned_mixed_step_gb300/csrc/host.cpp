@@ -58,7 +58,8 @@ size_t norm_ws_bytes(int64_t ranks, const NormGeom &g)
 }
 
 NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_units, int64_t nb,
-                   int64_t b0, int64_t nbl, int32_t ranks, void *ws, double *total)
+                   int64_t b0, int64_t nbl, int32_t ranks, int64_t counter_slots, void *ws,
+                   double *total)
 {
     NormPlan p{};
     p.cu = g.cu;
@@ -78,7 +79,7 @@ NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_un
     char *base = static_cast<char *>(ws);
     p.done = reinterpret_cast<uint32_t *>(base);
     p.sc_count = reinterpret_cast<uint32_t *>(base + kWsHeader);
-    const int64_t counters = round_up((int64_t)ranks * g.spr * (int64_t)sizeof(uint32_t), 256);
+    const int64_t counters = round_up(counter_slots * (int64_t)sizeof(uint32_t), 256);
     p.partials = reinterpret_cast<double *>(base + kWsHeader + counters);
     p.sc_partials = p.partials + (int64_t)ranks * g.cpr;
     p.total = total ? total : norm_total_slot(ws);

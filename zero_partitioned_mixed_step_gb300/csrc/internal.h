@@ -74,10 +74,16 @@ struct NormPlan {
 
 // The plan of a launch over buckets [b0, b0 + nbl) of nb (slices of
 // slice_units / last_slice_units units), forming the sums of `ranks` ranks,
-// with the tree in workspace `ws` (laid out for `ranks` ranks); the total goes
-// to `total`, or to the workspace's result slot when `total` is null.
+// with the tree in workspace `ws`; the total goes to `total`, or to the
+// workspace's result slot when `total` is null.  The counters occupy the
+// first counter_slots 4-byte slots after the header, whatever the launch:
+// every call on one workspace must pass the same counter_slots (the most any
+// of its calls uses), because only counters are relied on to be zero when a
+// call starts (each call returns the ones it uses to zero; the sums are
+// written before they are read).
 NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_units, int64_t nb,
-                   int64_t b0, int64_t nbl, int32_t ranks, void *ws, double *total);
+                   int64_t b0, int64_t nbl, int32_t ranks, int64_t counter_slots, void *ws,
+                   double *total);
 // Bytes zero_grad_norm needs for a vector of any length (one rank, one slice:
 // at most kNormChunksPerRank chunks, as the chunk grows with the vector).
 constexpr size_t kNormWsAnyVector =

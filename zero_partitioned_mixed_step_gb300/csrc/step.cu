@@ -643,15 +643,17 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
 }
 
 // The norm's tree for launches over buckets [b0, b0 + nbl) of `L` (the whole
-// layout), in workspace ws.
+// layout), in workspace ws.  The counters are laid out for every rank of the
+// layout whatever the view, so a workspace serves every view of its layout.
 NormPlan layout_plan(const zero_layout &L, int rank, int64_t b0, int64_t nbl, void *ws)
 {
     const bool bucketed = L.bucket_numel > 0;
     const int64_t nb = bucketed ? L.num_buckets : 1;
     const int64_t su = (bucketed ? L.slice_numel : L.owned_numel) / kUnit;
     const int64_t lsu = L.last_slice_numel / kUnit;
-    return norm_plan(norm_geometry(su, lsu, nb), su, lsu, nb, b0, nbl,
-                     rank < 0 ? L.world : 1, ws, nullptr);
+    const NormGeom g = norm_geometry(su, lsu, nb);
+    return norm_plan(g, su, lsu, nb, b0, nbl, rank < 0 ? L.world : 1, (int64_t)L.world * g.spr,
+                     ws, nullptr);
 }
 
 // Polls of the staged kernel's stage waits; a test may lower the limit with
