@@ -528,13 +528,17 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
-def run_e2e(z, grads, wl, args, steps: int = 5):
+def run_e2e(z, grads, wl, args, steps: int = 20):
     """End to end through ZeroStep.step_from_host: every rank's gradient sits
     in page-locked host memory (the library's zero_host_alloc blocks) and the
     step's kernels load it over the host link (zero-copy: every step moves
     the gradients host -> device inside the timed region; with offloaded
     state they are copied in first), then the step state is read back to the
-    host; all timed."""
+    host; each of `steps` steps is timed on its own with the host clock (the
+    call returns after the state has reached the host).  The value is the
+    median step's rate; min and max of the rate and the link rate of the same
+    steps are reported beside it (the host link is shared with the rest of
+    the machine and its rate moves from run to run)."""
     import torch
     import zero_partitioned_mixed_step_gb300 as zs
     try:
@@ -550,16 +554,20 @@ def run_e2e(z, grads, wl, args, steps: int = 5):
     dev = grads if wl.offload_state else None
     z.step_from_host(host, dev, stream, wl.micro_steps)  # warm-up
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    times = []
     for _ in range(steps):
+        t0 = time.perf_counter()
         z.step_from_host(host, dev, stream, wl.micro_steps)
-    el = time.perf_counter() - t0
+        times.append(time.perf_counter() - t0)
     h2d = sum(g.numel() * g.element_size() for g in grads) * wl.micro_steps
     params = wl.numel if wl.rank is None else min(z.layout.owned_numel, wl.numel)
     del host
-    return {"value": params * steps / el / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": 64, "steps": steps,
-            "link_gbs": h2d * steps / el / 1e9,
+    med = statistics.median(times)
+    return {"value": params / med / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": 64, "steps": steps, "stat": "median of per-step rates",
+            "min": params / max(times) / 1e9, "max": params / min(times) / 1e9,
+            "link_gbs": h2d / med / 1e9, "link_gbs_min": h2d / max(times) / 1e9,
+            "link_gbs_max": h2d / min(times) / 1e9,
             "h2d": ("copied into device buffers, then the step" if wl.offload_state else
                     "the step's kernels load the gradients from page-locked host memory")}
 

@@ -137,16 +137,9 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     norm_kernel(const float *g, int64_t n, float inv_s, NormPlan np)
 {
-    __shared__ NormShared nsh;
-    if (threadIdx.x == 0)
-        nsh.final_pending = 0;
-    __syncthreads();
     const int64_t full = n / kUnit;
-    SumSq ss;
-    int parity = 0;
-    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x, parity ^= 1) {
-        const ChunkLoc L = locate_chunk(np, pi);
-        ss.acc = FF{0.0f, 0.0f};
+    norm_walk(np, [&](const ChunkLoc &L) {
+        SumSq ss;
         for (int64_t k = threadIdx.x; k < L.n_u; k += kThreads) {
             const int64_t u = L.u0 + k;
             float x[8];
@@ -162,10 +155,8 @@ __global__ void __launch_bounds__(kThreads)
                 x[i] = __fmul_rn(x[i], inv_s);
             ss.add8(x);
         }
-        norm_chunk_done(np, L, ss.acc, parity, nsh);
-    }
-    __syncthreads();
-    norm_finish(np, nsh);
+        return ss.acc;
+    });
 }
 
 // zero_grad_norm's launch with the tree in `ws` (a workspace of at least

@@ -73,8 +73,8 @@ NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_un
     p.b0 = b0;
     p.nbl = nbl;
     const bool has_last = b0 + nbl == nb;
-    p.launch_chunks = (int64_t)ranks * ((nbl - (has_last ? 1 : 0)) * g.cps +
-                                        (has_last ? g.cps_last : 0));
+    p.rank_chunks = (nbl - (has_last ? 1 : 0)) * g.cps + (has_last ? g.cps_last : 0);
+    p.launch_chunks = (int64_t)ranks * p.rank_chunks;
     p.ranks = ranks;
     char *base = static_cast<char *>(ws);
     p.done = reinterpret_cast<uint32_t *>(base);

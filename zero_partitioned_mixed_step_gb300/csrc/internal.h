@@ -29,9 +29,10 @@ int check_cfg(const zero_adam_cfg *cfg);
 //   chunk      kNormChunkMinUnits .. units of one rank's slice of one bucket
 //              (chunks restart at every slice boundary), summed by one CTA in
 //              a fixed order: thread t takes units t, t + 256, ..., then a
-//              fixed tree over the threads;
+//              fixed butterfly inside each warp, then the warps in order;
 //   superchunk kNormSuper consecutive chunks of one rank, summed in a fixed
-//              lane order by the CTA that finishes the superchunk's last chunk;
+//              lane order by the CTA that holds all of them, or else by the
+//              CTA whose chunks complete the superchunk's count;
 //   rank       its superchunks in a fixed lane order;
 //   total      the ranks' sums added in ascending rank order from +0.
 // One rank's view forms its own rank sum only; an every-rank launch gives
@@ -62,7 +63,8 @@ struct NormPlan {
     int64_t slice_units, last_slice_units;  // of the whole layout
     int64_t nb;             // buckets of the whole layout
     int64_t b0, nbl;        // the launch covers buckets b0 .. b0 + nbl - 1
-    int64_t launch_chunks;  // chunks the launch computes
+    int64_t rank_chunks;    // chunks of each rank the launch computes
+    int64_t launch_chunks;  // chunks the launch computes (ranks x rank_chunks)
     int32_t ranks;          // ranks whose sums are formed (world, or 1 for one rank's view)
     int32_t pad_;
     uint32_t *done;         // superchunks finished (shared by all launches of a step)

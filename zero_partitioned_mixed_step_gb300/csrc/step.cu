@@ -95,18 +95,12 @@ struct StepParams {
 
 // A first pass's walk over its chunks of the norm's tree: each chunk's units
 // go through `unit` (which adds their squares to ss), then the chunk's sum
-// enters the tree; the CTA that completes the tree finishes it.
+// enters the tree (norm_walk in kernels.cuh).
 template <bool ALL, class UnitFn>
 __device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, SumSq &ss,
                                           UnitFn &unit)
 {
-    __shared__ NormShared nsh;
-    if (threadIdx.x == 0)
-        nsh.final_pending = 0;
-    __syncthreads();
-    int parity = 0;
-    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x, parity ^= 1) {
-        const ChunkLoc L = locate_chunk(np, pi);
+    norm_walk(np, [&](const ChunkLoc &L) {
         int64_t ubase;  // the launch's unit index of the chunk's first unit
         if constexpr (ALL) {
             int64_t flat;
@@ -121,10 +115,8 @@ __device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, Su
         ss.acc = FF{0.0f, 0.0f};
         for (int64_t k = threadIdx.x; k < L.n_u; k += kThreads)
             unit(ubase + k);
-        norm_chunk_done(np, L, ss.acc, parity, nsh);
-    }
-    __syncthreads();
-    norm_finish(np, nsh);
+        return ss.acc;
+    });
 }
 
 // The body of the streaming kernels (the __global__ wrappers below differ
