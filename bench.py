@@ -423,8 +423,9 @@ def run_ours(args, wl):
                 join()
 
             bucket0 = []
-            if clip:  # first pass on every bucket, then the second pass on every bucket
+            if clip:  # first pass on every bucket, the norm, the second pass on every bucket
                 buckets(lambda b, st: z.pass1_buckets(grads, b, 1, st))
+                z.norm_buckets(stream)
                 bucket0.clear()
                 buckets(lambda b, st: z.pass2_buckets(grads, b, 1, st))
             else:
@@ -481,12 +482,13 @@ def run_ours(args, wl):
     peak = peaks["hbm_gbs"]
     traffic = recorded_traffic(wl.name)
     rate, threads, desc = oracle_sample_rate(wl)
-    # the step's last kernel also ends the step: one launch per pass, plus one
-    # per accumulated micro-step
-    launches_per_step = (2 if clip else 1) + (wl.micro_steps if wl.micro_steps > 1 else 0)
+    # the step's last kernel also ends the step: one launch per pass (and the
+    # norm's tree kernel between the passes of a clipped step), plus one per
+    # accumulated micro-step
+    launches_per_step = (3 if clip else 1) + (wl.micro_steps if wl.micro_steps > 1 else 0)
     pipeline = {}
     if wl.per_bucket:
-        launches_per_step = (2 if clip else 1) * L.num_buckets + 1
+        launches_per_step = (2 * L.num_buckets + 2) if clip else (L.num_buckets + 1)
         firsts = [a.elapsed_time(f) for (a, _), f in zip(ev, first_bucket_done)]
         pipeline = {"pipeline": {"buckets": L.num_buckets, "streams": 2,
                                  "passes": 2 if clip else 1,

@@ -213,18 +213,16 @@ ZERO_API int zero_state_init(zero_step_state *host_state, float loss_scale);
  * Bytes of device workspace a step on `layout` needs (zero_step_fused,
  * zero_step_fused_accumulated, zero_step_buckets_pass1 / _pass2), or, with
  * layout = NULL, the bytes zero_grad_norm needs for a vector of any length
- * (268,544).  0 for an invalid layout.
+ * (2,101,504).  0 for an invalid layout.
  * The workspace holds the tree over which the global sum of squares is
  * formed: chunks of at least 4096 elements of one rank's slice of one bucket
- * (about 32768 chunks per rank for large partitions), 64 chunks to a
- * superchunk, then ranks; its size is about 8 bytes per 4096 elements (a
- * few MB for billions of parameters).  Its shape depends only on the layout,
- * so the sum's bits do not depend on the GPU, the grid, or how the buckets
- * are split into ranges.  It also holds counters: ZERO-FILL THE WORKSPACE
- * ONCE before its first use; every call that runs to completion leaves the
- * counters at zero again.  A workspace serves the steps of one layout (every
- * rank's view of it), or zero_grad_norm: its counters sit where the calls of
- * that one use expect them.
+ * (about 32768 chunks per rank for large partitions), each summed as 8 warp
+ * leaves; 64 chunks to a superchunk; then ranks.  It takes about 64 bytes per
+ * chunk (16 MB for 8 billion parameters over 8 ranks).  Its shape depends
+ * only on the layout, so the sum's bits do not depend on the GPU, the grid,
+ * or how the buckets are split into ranges.  ZERO-FILL THE WORKSPACE ONCE
+ * before its first use: it holds one counter, which every call that runs to
+ * completion returns to zero.
  */
 ZERO_API size_t zero_workspace_bytes(const zero_layout *layout);
 
@@ -289,7 +287,8 @@ ZERO_API int zero_check_overflow(const float *g, int64_t n, float inv_scale, int
  * Relative error about 1e-13 or better.  g: device, 32-byte aligned;
  * sumsq_dev: device double; ws: device workspace of ws_bytes >=
  * zero_workspace_bytes(NULL), zero-filled before its first use (the call
- * leaves its counters at zero).  One launch (none for n = 0: *sumsq_dev = 0).
+ * leaves its counter at zero).  Two launches: the leaves, then the tree (a
+ * memset for n = 0: *sumsq_dev = +0).
  * Pages: "zero-optimizer", "一. 优化前" (gradient-norm computation over fused
  * buffers); the clip rule itself is a reading (see zero_adam_cfg).
  */
@@ -344,19 +343,19 @@ ZERO_API int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
  *  Result, arguments and summation order: as zero_grad_norm (the same kernel
  *  and the same tree, so the same bits), without ws / ws_bytes.
  *  Scratch: the tree lives in a library-owned static device array of
- *  ZERO_NOALLOC_SCRATCH_BYTES (268,544 bytes: the tree of a vector of any
+ *  ZERO_NOALLOC_SCRATCH_BYTES (2,101,504 bytes: the tree of a vector of any
  *  length) that every GPU which loads the library holds until the process
  *  exits.  A vector whose tree would not fit is rejected with ZERO_ESPACE
- *  (none is: the chunks grow with the vector).  The array's counters are zero
- *  when the library is loaded and every call returns them to zero; the other
- *  slots are written before they are read.  All calls share the array, so
+ *  (none is: the chunks grow with the vector).  The array's one counter is
+ *  zero when the library is loaded and every call returns it to zero; the
+ *  other slots are written before they are read.  All calls share the array, so
  *  calls that can overlap on the GPU (different streams, or different host
  *  threads, without ordering between them) race and must not be issued.
  *  Set-up: the first call on each device looks up the array's device
  *  address for the current device (cudaGetSymbolAddress) and caches it; make
  *  that first call before any stream capture.
  */
-#define ZERO_NOALLOC_SCRATCH_BYTES 268544
+#define ZERO_NOALLOC_SCRATCH_BYTES 2101504
 ZERO_API int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *sumsq_dev,
                                     zero_stream_t stream);
 
@@ -473,19 +472,21 @@ ZERO_API int zero_step_fused_buckets(const void *const *grads, int grads_are_sli
  *   1. zero_step_buckets_pass1 on every bucket of the layout, exactly once,
  *      in ranges [first_bucket, first_bucket + n_buckets): (a2) reduce, (a3)
  *      unscale, (a4) flag NaN/Inf in state_dev->found_inf, (a5) the squares'
- *      sums into the workspace's fixed tree, and, with g_stage, keep the
+ *      leaves into the workspace's fixed tree, and, with g_stage, keep the
  *      unscaled gradient there.  A range can run as soon as its buckets'
  *      gradients are ready (during the backward pass), and ranges may run
- *      concurrently on different streams.  The launch that completes the
- *      tree's last superchunk (whichever range that is) adds the ranks' sums
- *      in ascending rank order and stores the total in the workspace.
- *   2. zero_step_buckets_pass2 on every bucket, exactly once, in ranges,
- *      each on a stream ordered after EVERY pass-1 range: (a5) the clip with
- *      c = min(1, max_norm / (sqrt(total) + 1e-6)), (a6) Adam/AdamW, (a7) the
- *      cast; a range's parameters are final (ready for its all-gather) as
- *      soon as the range completes.  Skipped (nothing written) when pass 1
- *      flagged NaN/Inf.  The ranges may run concurrently.
- *   3. zero_step_finalize(cfg, state_dev, 1, stream) after every pass-2 range:
+ *      concurrently on different streams.
+ *   2. zero_step_buckets_norm once, on a stream ordered after EVERY pass-1
+ *      range: the tree above the leaves in its fixed order (chunks,
+ *      superchunks, each rank, then the ranks in ascending order) gives the
+ *      global sum of squares, kept in the workspace.
+ *   3. zero_step_buckets_pass2 on every bucket, exactly once, in ranges, each
+ *      on a stream ordered after step 2: (a5) the clip with c = min(1,
+ *      max_norm / (sqrt(total) + 1e-6)), (a6) Adam/AdamW, (a7) the cast; a
+ *      range's parameters are final (ready for its all-gather) as soon as the
+ *      range completes.  Skipped (nothing written) when pass 1 flagged
+ *      NaN/Inf.  The ranges may run concurrently.
+ *   4. zero_step_finalize(cfg, state_dev, 1, stream) after every pass-2 range:
  *      commits (t + 1, cur toggled) or skips the step.
  * The result is bit for bit that of zero_step_fused with the clip on the
  * same buffers, whatever the split into ranges, and state_dev->sumsq /
@@ -500,17 +501,19 @@ ZERO_API int zero_step_fused_buckets(const void *const *grads, int grads_are_sli
  *    gradient there and pass 2 reads it.  Pass 2 takes exactly one source:
  *    grads (reduced again) or g_stage.
  *  ws, ws_bytes: the step's workspace (zero_workspace_bytes(layout),
- *    zero-filled before first use), the same for every range of the step.
+ *    zero-filled before first use), the same for every call of the step.
  *  master/m/v/params (pass 2): ping-pong slots as zero_step_fused; they may
  *    alias (in place), and must be device memory.
- * Every bucket must go through each pass exactly once per step: a bucket left
- * out of pass 1 leaves the tree's counters short, and no total is formed.
+ * Every bucket must go through each pass exactly once per step; a bucket left
+ * out of pass 1 leaves stale leaves in the tree.
  */
 ZERO_API int zero_step_buckets_pass1(const void *const *grads, int grads_are_slices,
                                      zero_dtype dtype, const zero_layout *layout, int rank,
                                      int64_t first_bucket, int64_t n_buckets, float *g_stage,
                                      const zero_adam_cfg *cfg, zero_step_state *state_dev,
                                      void *ws, size_t ws_bytes, zero_stream_t stream);
+ZERO_API int zero_step_buckets_norm(const zero_layout *layout, int rank, void *ws,
+                                    size_t ws_bytes, zero_stream_t stream);
 ZERO_API int zero_step_buckets_pass2(const void *const *grads, int grads_are_slices,
                                      zero_dtype dtype, const zero_layout *layout, int rank,
                                      int64_t first_bucket, int64_t n_buckets,

@@ -204,11 +204,13 @@ def step_group(z, grads, wl, check_split=False):
         whole = None
         if check_split:
             z.pass1_buckets(grads, 0, nb, s0)
+            z.norm_buckets(s0)
             whole = _ws_total(z)
         fork()
         for b in range(nb):
             z.pass1_buckets(grads, b, 1, side[b % 2])
         join()
+        z.norm_buckets(s0)
         if check_split:
             assert _ws_total(z) == whole
         fork()

@@ -9,7 +9,7 @@ slices, superchunks, ranks in ascending order), so:
     sums, as an all-reduce of per-rank sums in rank order would give it,
     and zero_grad_norm of a rank's reduced gradient is that rank's sum;
   * splitting the clipped step into bucket ranges on two streams (pass 1 on
-    every range, then pass 2 on every range, then the commit) gives the
+    every range, the norm, pass 2 on every range, the commit) gives the
     fused step's bits, including a step skipped for an Inf in a middle
     bucket ("DeepSpeed ZeRO", ZeRO Stage 1: overlap of the optimizer step
     with the all-gather, over the constant-size buffers of "相关分析")."""
@@ -133,6 +133,7 @@ def test_clipped_bucket_ranges_equal_fused_step(name):
         for i, (f, n) in enumerate(ranges):
             alt.z.pass1_buckets(gd, f, n, side[i % 2])
         join()
+        alt.z.norm_buckets(s0)
         fork()
         for i, (f, n) in enumerate(reversed(ranges)):
             alt.z.pass2_buckets(gd, f, n, side[i % 2])

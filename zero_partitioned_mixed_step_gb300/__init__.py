@@ -11,7 +11,7 @@ Entry points (same names as the C ABI):
   zero_grad_norm_noalloc, zero_adam_step, zero_step_finalize,
   zero_step_fused, zero_reduce_scatter_accumulate,
   zero_step_fused_accumulated, zero_step_fused_buckets,
-  zero_step_buckets_pass1, zero_step_buckets_pass2.
+  zero_step_buckets_pass1, zero_step_buckets_norm, zero_step_buckets_pass2.
 ``ZeroStep`` owns the buffers of one simulated data-parallel group and runs
 the fused step on them.
 """
@@ -32,7 +32,8 @@ __all__ = [
     "zero_state_init", "zero_workspace_bytes", "zero_reduce_scatter_sum", "zero_check_overflow",
     "zero_grad_norm", "zero_grad_norm_noalloc", "zero_adam_step", "zero_step_finalize", "zero_step_fused",
     "zero_reduce_scatter_accumulate", "zero_step_fused_accumulated", "zero_step_fused_buckets",
-    "zero_step_buckets_pass1", "zero_step_buckets_pass2", "host_empty",
+    "zero_step_buckets_pass1", "zero_step_buckets_norm", "zero_step_buckets_pass2",
+    "host_empty",
 ]
 
 _TORCH_DT = {F16: torch.float16, BF16: torch.bfloat16}
@@ -274,6 +275,15 @@ def zero_step_buckets_pass1(grads: Sequence[torch.Tensor], layout: Layout, first
                                         ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def zero_step_buckets_norm(layout: Layout, ws: torch.Tensor, rank: int = -1,
+                           stream=None) -> None:
+    """The clipped step's global sum of squares, after the first pass on
+    every bucket and before the second pass on any."""
+    check("zero_step_buckets_norm",
+          lib().zero_step_buckets_norm(ctypes.byref(layout), rank, _dev_ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def zero_step_buckets_pass2(grads: Optional[Sequence[torch.Tensor]], layout: Layout,
                             first_bucket: int, n_buckets: int, master: Sequence[torch.Tensor],
                             m: Sequence[torch.Tensor], v: Sequence[torch.Tensor],
@@ -414,6 +424,10 @@ class ZeroStep:
         zero_step_buckets_pass1(grads, self.layout, first_bucket, n_buckets, self.cfg,
                                 self.state, self.ws, self.rank, self.g_stage,
                                 self.grads_are_slices, stream, self.half_reduce)
+
+    def norm_buckets(self, stream=None) -> None:
+        """The clipped step's global norm, between the two passes."""
+        zero_step_buckets_norm(self.layout, self.ws, self.rank, stream)
 
     def pass2_buckets(self, grads: Optional[Sequence[torch.Tensor]], first_bucket: int,
                       n_buckets: int, stream=None) -> None:

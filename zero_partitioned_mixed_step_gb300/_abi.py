@@ -15,7 +15,7 @@ EALIGN = -2
 ESPACE = -3
 ECUDA_BASE = -1000
 MAX_WORLD = 1024
-NOALLOC_SCRATCH_BYTES = 268544
+NOALLOC_SCRATCH_BYTES = 2101504
 
 
 class Layout(ctypes.Structure):
@@ -75,6 +75,7 @@ SIGNATURES = {
                                      ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P], _I),
     "zero_step_buckets_pass1": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _I64, _I64, _P,
                                  ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P], _I),
+    "zero_step_buckets_norm": ([ctypes.POINTER(Layout), _I, _P, ctypes.c_size_t, _P], _I),
     "zero_step_buckets_pass2": ([_P, _I, _I, ctypes.POINTER(Layout), _I, _I64, _I64, _P, _P, _P,
                                  _P, _P, ctypes.POINTER(AdamCfg), _P, _P, ctypes.c_size_t, _P],
                                 _I),

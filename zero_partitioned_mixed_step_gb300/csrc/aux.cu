@@ -131,9 +131,79 @@ __global__ void __launch_bounds__(kThreads)
     flag_nonfinite(bad, flag);
 }
 
-// The sum of squares of g * inv_s over the norm's fixed tree (internal.h),
-// the vector taken as one rank's single slice of ceil(n / 8) units (the last
-// one padded with zeros); the CTA that completes the tree writes the total.
+// The tree above the leaves that a first pass (or the first passes of all
+// the bucket ranges of a step) stored: every warp sums superchunks (lane l
+// takes chunks l and l + 32 of the superchunk, each the sum of its leaves in
+// warp order, then a fixed butterfly); the CTA that finishes last adds each
+// rank's superchunks (the same lane order) and then the ranks in ascending
+// order from +0, writes the total and returns the counter to zero.
+__global__ void __launch_bounds__(kThreads) norm_tree_kernel(NormPlan np)
+{
+    __shared__ double rank_sum[ZERO_MAX_WORLD];
+    __shared__ int last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t nsc = (int64_t)np.ranks * np.spr;
+    const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t sc = (int64_t)blockIdx.x * (kThreads / 32) + warp; sc < nsc; sc += warps) {
+        const int64_t r = sc / np.spr, s = sc - r * np.spr;
+        const int64_t c0 = r * np.cpr + s * kNormSuper;
+        const int64_t left = np.cpr - s * kNormSuper;
+        const int64_t size = left < kNormSuper ? left : kNormSuper;
+        double x = 0.0;
+        for (int64_t j = lane; j < size; j += 32) {
+            const float2 *lf = np.leaves + (c0 + j) * kNormLeaves;
+            float2 v[kNormLeaves];
+#pragma unroll
+            for (int w = 0; w < kNormLeaves; ++w)
+                v[w] = __ldcg(lf + w);
+            FF t{v[0].x, v[0].y};
+#pragma unroll
+            for (int w = 1; w < kNormLeaves; ++w)
+                t = ff_add(t, FF{v[w].x, v[w].y});
+            x = __dadd_rn(x, __dadd_rn((double)t.hi, (double)t.lo));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+        if (lane == 0)
+            np.sc_partials[sc] = x;
+    }
+    __threadfence();  // this CTA's superchunk sums before its count
+    __syncthreads();
+    if (threadIdx.x == 0)
+        last = atomicAdd(np.done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last)
+        return;
+    __threadfence();
+    for (int r = warp; r < np.ranks; r += kThreads / 32) {
+        const double x = warp_fixed_sum(np.sc_partials + (int64_t)r * np.spr, np.spr);
+        if (lane == 0)
+            rank_sum[r] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double total = 0.0;
+        for (int r = 0; r < np.ranks; ++r)
+            total = __dadd_rn(total, rank_sum[r]);
+        *np.total = total;
+        *np.done = 0u;
+    }
+}
+
+int launch_norm_tree(const NormPlan &np, cudaStream_t stream)
+{
+    const int64_t nsc = (int64_t)np.ranks * np.spr;
+    const int64_t want = (nsc + kThreads / 32 - 1) / (kThreads / 32);
+    const int target = target_ctas(reinterpret_cast<const void *>(norm_tree_kernel));
+    const int gx = (int)(want < 1 ? 1 : (want < target ? want : target));
+    norm_tree_kernel<<<gx, kThreads, 0, stream>>>(np);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+}
+
+// The leaves of the sum of squares of g * inv_s, the vector taken as one
+// rank's single slice of ceil(n / 8) units (the last one padded with zeros).
 __global__ void __launch_bounds__(kThreads)
     norm_kernel(const float *g, int64_t n, float inv_s, NormPlan np)
 {
@@ -159,8 +229,8 @@ __global__ void __launch_bounds__(kThreads)
     });
 }
 
-// zero_grad_norm's launch with the tree in `ws` (a workspace of at least
-// norm_ws_bytes_any_vector() bytes whose counters are zero).
+// zero_grad_norm's two launches (the leaves, then the tree) with the tree in
+// `ws`, a workspace of ws_bytes bytes whose counter is zero.
 static int launch_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
                        size_t ws_bytes, cudaStream_t stream)
 {
@@ -170,19 +240,16 @@ static int launch_norm(const float *g, int64_t n, float inv_scale, double *sumsq
     }
     const int64_t units = (n + kUnit - 1) / kUnit;
     const NormGeom geo = norm_geometry(units, units, 1);
-    const size_t need = kWsHeader + (kNormChunksPerRank / kNormSuper) * sizeof(uint32_t) +
-                        (size_t)(geo.cpr + geo.spr) * sizeof(double);
-    if (need > ws_bytes)
+    if (norm_ws_bytes(1, geo) > ws_bytes)
         return ZERO_ESPACE;
-    // the counters of the longest vector's tree, so any sequence of lengths
-    // finds its counters at zero
-    const NormPlan np = norm_plan(geo, units, units, 1, 0, 1, 1,
-                                  kNormChunksPerRank / kNormSuper, ws, sumsq_dev);
+    const NormPlan np = norm_plan(geo, units, units, 1, 0, 1, 1, ws, sumsq_dev);
     const int target = target_ctas(reinterpret_cast<const void *>(norm_kernel));
     const int gx = (int)(np.launch_chunks < target ? np.launch_chunks : target);
     norm_kernel<<<gx, kThreads, 0, stream>>>(g, n, inv_scale, np);
     const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ZERO_OK : cuda_error(e);
+    if (e != cudaSuccess)
+        return cuda_error(e);
+    return launch_norm_tree(np, stream);
 }
 
 template <int DT>
@@ -322,9 +389,8 @@ namespace zs {
 static_assert(kNormWsAnyVector == ZERO_NOALLOC_SCRATCH_BYTES,
               "the static scratch holds the tree of any vector");
 
-// The tree of one call: counters (zero when the library is loaded, and
-// returned to zero by every call that completes), chunk and superchunk sums
-// and the result slot.  Every GPU that loads the library holds this array
+// The tree of one call: its counter (zero when the library is loaded, and
+// returned to zero by every call that completes), leaves and superchunk sums.  Every GPU that loads the library holds this array
 // until the process exits.  In host code the name is only a host-side
 // stand-in for the device array: kernels must be given the address
 // cudaGetSymbolAddress returns for the current device.

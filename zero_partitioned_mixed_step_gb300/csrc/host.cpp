@@ -4,6 +4,7 @@
 #include <cstring>
 
 #include <cuda_runtime.h>
+#include <vector_types.h>
 
 #include "internal.h"
 
@@ -52,14 +53,12 @@ NormGeom norm_geometry(int64_t slice_units, int64_t last_slice_units, int64_t nb
 
 size_t norm_ws_bytes(int64_t ranks, const NormGeom &g)
 {
-    const int64_t counters = round_up(ranks * g.spr * (int64_t)sizeof(uint32_t), 256);
-    return (size_t)(kWsHeader + counters + ranks * g.cpr * (int64_t)sizeof(double) +
+    return (size_t)(kWsHeader + ranks * g.cpr * kNormLeaves * (int64_t)sizeof(float2) +
                     ranks * g.spr * (int64_t)sizeof(double));
 }
 
 NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_units, int64_t nb,
-                   int64_t b0, int64_t nbl, int32_t ranks, int64_t counter_slots, void *ws,
-                   double *total)
+                   int64_t b0, int64_t nbl, int32_t ranks, void *ws, double *total)
 {
     NormPlan p{};
     p.cu = g.cu;
@@ -73,15 +72,13 @@ NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_un
     p.b0 = b0;
     p.nbl = nbl;
     const bool has_last = b0 + nbl == nb;
-    p.rank_chunks = (nbl - (has_last ? 1 : 0)) * g.cps + (has_last ? g.cps_last : 0);
-    p.launch_chunks = (int64_t)ranks * p.rank_chunks;
+    p.launch_chunks = (int64_t)ranks * ((nbl - (has_last ? 1 : 0)) * g.cps +
+                                        (has_last ? g.cps_last : 0));
     p.ranks = ranks;
     char *base = static_cast<char *>(ws);
     p.done = reinterpret_cast<uint32_t *>(base);
-    p.sc_count = reinterpret_cast<uint32_t *>(base + kWsHeader);
-    const int64_t counters = round_up(counter_slots * (int64_t)sizeof(uint32_t), 256);
-    p.partials = reinterpret_cast<double *>(base + kWsHeader + counters);
-    p.sc_partials = p.partials + (int64_t)ranks * g.cpr;
+    p.leaves = reinterpret_cast<float2 *>(base + kWsHeader);
+    p.sc_partials = reinterpret_cast<double *>(p.leaves + (int64_t)ranks * g.cpr * kNormLeaves);
     p.total = total ? total : norm_total_slot(ws);
     return p;
 }

@@ -3,6 +3,8 @@
 
 #include <cstdint>
 
+#include <vector_types.h>
+
 #include "zerostep.h"
 
 namespace zs {
@@ -26,20 +28,24 @@ int check_cfg(const zero_adam_cfg *cfg);
 // The global sum of squares is formed over a tree whose shape depends only on
 // the layout (never on the device or the grid), so every launch shape, every
 // split of the buckets into ranges and every GPU give the same bits:
-//   chunk      kNormChunkMinUnits .. units of one rank's slice of one bucket
-//              (chunks restart at every slice boundary), summed by one CTA in
-//              a fixed order: thread t takes units t, t + 256, ..., then a
-//              fixed butterfly inside each warp, then the warps in order;
-//   superchunk kNormSuper consecutive chunks of one rank, summed in a fixed
-//              lane order by the CTA that holds all of them, or else by the
-//              CTA whose chunks complete the superchunk's count;
+//   leaf       one warp's share of a chunk: a chunk is kNormChunkMinUnits ..
+//              units of one rank's slice of one bucket (chunks restart at
+//              every slice boundary), summed by one CTA: thread t takes units
+//              t, t + 256, ...; each warp adds its lanes with a fixed
+//              butterfly and stores the pair;
+//   chunk      its 8 leaves in warp order;
+//   superchunk kNormSuper consecutive chunks of one rank, in a fixed lane
+//              order;
 //   rank       its superchunks in a fixed lane order;
 //   total      the ranks' sums added in ascending rank order from +0.
-// One rank's view forms its own rank sum only; an every-rank launch gives
-// exactly the rank-order sum of the per-rank results.
+// The first pass stores leaves only (no synchronisation between CTAs); the
+// tree kernel (launch_norm_tree) forms the rest.  One rank's view forms its
+// own rank sum only; an every-rank launch gives exactly the rank-order sum of
+// the per-rank results.
 constexpr int64_t kNormChunkMinUnits = 512;      // 4096 elements
 constexpr int64_t kNormChunksPerRank = 32768;    // target upper bound per rank
 constexpr int kNormSuper = 64;                   // chunks per superchunk
+constexpr int kNormLeaves = kThreads / 32;       // leaves (warps) per chunk
 
 // Chunk geometry of one rank's elements.
 struct NormGeom {
@@ -63,13 +69,11 @@ struct NormPlan {
     int64_t slice_units, last_slice_units;  // of the whole layout
     int64_t nb;             // buckets of the whole layout
     int64_t b0, nbl;        // the launch covers buckets b0 .. b0 + nbl - 1
-    int64_t rank_chunks;    // chunks of each rank the launch computes
-    int64_t launch_chunks;  // chunks the launch computes (ranks x rank_chunks)
+    int64_t launch_chunks;  // chunks the launch computes
     int32_t ranks;          // ranks whose sums are formed (world, or 1 for one rank's view)
     int32_t pad_;
-    uint32_t *done;         // superchunks finished (shared by all launches of a step)
-    uint32_t *sc_count;     // chunks finished, per superchunk
-    double *partials;       // chunk sums
+    uint32_t *done;         // the tree kernel's finished CTAs (zero between launches)
+    float2 *leaves;         // kNormLeaves (hi, lo) pairs per chunk
     double *sc_partials;    // superchunk sums
     double *total;          // where the total goes
 };
@@ -77,26 +81,23 @@ struct NormPlan {
 // The plan of a launch over buckets [b0, b0 + nbl) of nb (slices of
 // slice_units / last_slice_units units), forming the sums of `ranks` ranks,
 // with the tree in workspace `ws`; the total goes to `total`, or to the
-// workspace's result slot when `total` is null.  The counters occupy the
-// first counter_slots 4-byte slots after the header, whatever the launch:
-// every call on one workspace must pass the same counter_slots (the most any
-// of its calls uses), because only counters are relied on to be zero when a
-// call starts (each call returns the ones it uses to zero; the sums are
-// written before they are read).
+// workspace's result slot when `total` is null.  Only the counter at the
+// start of the workspace must be zero when a tree kernel starts (it returns
+// it to zero); every other slot is written before it is read.
 NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_units, int64_t nb,
-                   int64_t b0, int64_t nbl, int32_t ranks, int64_t counter_slots, void *ws,
-                   double *total);
+                   int64_t b0, int64_t nbl, int32_t ranks, void *ws, double *total);
 // Bytes zero_grad_norm needs for a vector of any length (one rank, one slice:
 // at most kNormChunksPerRank chunks, as the chunk grows with the vector).
-constexpr size_t kNormWsAnyVector =
-    kWsHeader + ((kNormChunksPerRank / kNormSuper) * 4 + 255) / 256 * 256 +
-    kNormChunksPerRank * 8 + (kNormChunksPerRank / kNormSuper) * 8;
+constexpr size_t kNormWsAnyVector = kWsHeader + kNormChunksPerRank * kNormLeaves * 8 +
+                                    (kNormChunksPerRank / kNormSuper) * 8;
 inline size_t norm_ws_bytes_any_vector() { return kNormWsAnyVector; }
-// The workspace's result slot (written by the last launch of a step's first pass).
+// The workspace's result slot (written by the tree kernel).
 inline double *norm_total_slot(void *ws)
 {
     return reinterpret_cast<double *>(static_cast<char *>(ws) + 8);
 }
+// The tree kernel: leaves -> chunks -> superchunks -> ranks -> total (aux.cu).
+int launch_norm_tree(const NormPlan &np, struct CUstream_st *stream);
 
 }  // namespace zs
 

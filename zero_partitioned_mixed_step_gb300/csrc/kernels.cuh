@@ -568,194 +568,68 @@ __device__ __forceinline__ double warp_fixed_sum(const double *p, int64_t n)
 
 // ------------------------------------------------------------------ the norm's tree
 //
-// Chunks, superchunks, ranks (see NormPlan in internal.h).  A launch's chunks
-// are numbered rank by rank, each rank's in its element order; CTA b of G
-// takes the contiguous run [b T / G, (b + 1) T / G) of the T chunks, so most
-// superchunks lie whole inside one CTA, which sums them from shared memory
-// with no synchronisation beyond one barrier per superchunk.  A superchunk
-// cut by a CTA's or a launch's edge is finished through a counter: the CTAs
-// holding parts of it store their chunk sums and add their chunk counts, and
-// the one whose addition completes the count sums it.  The CTA that brings
-// the count of finished superchunks to the total finishes the tree.
+// Leaves, chunks, superchunks, ranks (see NormPlan in internal.h).  A first
+// pass walks its chunks with a grid stride, so that at any moment the CTAs
+// stream neighbouring memory (every-rank launches take the chunks bucket by
+// bucket and rank by rank inside a bucket: the flat order); a whole CTA sums
+// one chunk, and each warp stores its leaf.  Nothing in the walk waits for
+// another warp or CTA.
 
-// Where a chunk lies.
+// Where a chunk lies and where its leaves go.
 struct ChunkLoc {
     int64_t r;        // rank, relative to the launch (0 for one rank's view)
     int64_t bl;       // bucket, relative to the launch
     int64_t u0, n_u;  // its units within the rank's slice of that bucket
-    int64_t k;        // its index among the rank's chunks
+    int64_t ci;       // its slot among the chunks (rank by rank, in element order)
 };
 
 __device__ __forceinline__ ChunkLoc locate_chunk(const NormPlan &np, int64_t pi)
 {
     ChunkLoc L;
     const bool has_last = np.b0 + np.nbl == np.nb;
-    const int64_t full = (np.nbl - (has_last ? 1 : 0)) * np.cps;
-    L.r = pi / np.rank_chunks;
-    const int64_t kl = pi - L.r * np.rank_chunks;
-    int64_t c, ub;
-    if (kl < full) {
-        L.bl = kl / np.cps;
-        c = kl - L.bl * np.cps;
+    const int64_t per_bucket = (int64_t)np.ranks * np.cps;
+    const int64_t n_full = (np.nbl - (has_last ? 1 : 0)) * per_bucket;
+    int64_t c, ub, k;
+    if (pi < n_full) {
+        L.bl = pi / per_bucket;
+        const int64_t rem = pi - L.bl * per_bucket;
+        L.r = rem / np.cps;
+        c = rem - L.r * np.cps;
         ub = np.slice_units;
+        k = (np.b0 + L.bl) * np.cps + c;
     } else {
+        const int64_t rem = pi - n_full;
+        L.r = rem / np.cps_last;
+        c = rem - L.r * np.cps_last;
         L.bl = np.nbl - 1;
-        c = kl - full;
         ub = np.last_slice_units;
+        k = (np.nb - 1) * np.cps + c;
     }
     L.u0 = c * np.cu;
     L.n_u = ub - L.u0 < np.cu ? ub - L.u0 : np.cu;
-    L.k = np.b0 * np.cps + kl;
+    L.ci = L.r * np.cpr + k;
     return L;
 }
 
-// warp_fixed_sum's order over values in shared memory (n <= 64).
-__device__ __forceinline__ double warp_fixed_sum_shared(const double *p, int n)
-{
-    const int lane = threadIdx.x & 31;
-    double x = 0.0;
-    for (int i = lane; i < n; i += 32)
-        x = __dadd_rn(x, p[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-    return x;
-}
-
-struct NormShared {
-    FF wsum[2][kNormSuper][kThreads / 32];  // warps' chunk sums, double-buffered by segment
-    double cp[kNormSuper];                  // a whole superchunk's chunk sums
-    uint32_t done_local;                    // superchunks this CTA finished
-    int final_pending;                      // this CTA finished the step's last superchunk
-};
-
-// Warp 0: superchunk sci's chunk sums are all in np.partials (written by the
-// CTAs that hold its chunks); sum them and count the superchunk as finished.
-__device__ __forceinline__ void finish_superchunk(const NormPlan &np, int64_t sci, int64_t sc0,
-                                                  int size, NormShared &sh)
-{
-    __threadfence();
-    const double x = warp_fixed_sum(np.partials + sc0, size);
-    if ((threadIdx.x & 31) == 0) {
-        np.sc_partials[sci] = x;
-        np.sc_count[sci] = 0u;
-        sh.done_local += 1;
-    }
-}
-
-// After every thread has passed the last barrier of the walk: if this CTA
-// finished the step's last superchunk, sum each rank's superchunks (warp w
-// takes ranks w, w + 8, ...), add the ranks in ascending order from +0, write
-// the total and reset the step's superchunk count.
-__device__ __forceinline__ void norm_finish(const NormPlan &np, NormShared &sh)
-{
-    __shared__ double rank_sum[ZERO_MAX_WORLD];
-    if (!sh.final_pending)
-        return;
-    __threadfence();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r < np.ranks; r += kThreads / 32) {
-        const double s = warp_fixed_sum(np.sc_partials + (int64_t)r * np.spr, np.spr);
-        if (lane == 0)
-            rank_sum[r] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double total = 0.0;
-        for (int r = 0; r < np.ranks; ++r)
-            total = __dadd_rn(total, rank_sum[r]);
-        *np.total = total;
-        *np.done = 0u;
-    }
-}
-
-// A launch's walk over its chunks of the tree, called by every thread.
-// chunk_fn(L) sums the squares of this thread's units of chunk L (units
-// L.u0 + threadIdx.x, + 256, ...) and returns the pair.
+// A first pass's walk over its chunks, called by every thread.  chunk_fn(L)
+// sums the squares of this thread's units of chunk L (units L.u0 +
+// threadIdx.x, + 256, ...) and returns the pair.
 template <class ChunkFn>
 __device__ __forceinline__ void norm_walk(const NormPlan &np, ChunkFn &&chunk_fn)
 {
-    __shared__ NormShared sh;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        sh.done_local = 0u;
-        sh.final_pending = 0;
-    }
-    __syncthreads();
-    const int64_t T = np.launch_chunks;
-    const int64_t lo = T * blockIdx.x / gridDim.x, hi = T * (blockIdx.x + 1) / gridDim.x;
-    int buf = 0;
-    for (int64_t pi = lo; pi < hi; buf ^= 1) {
-        // one segment: this CTA's chunks of one superchunk
-        const int64_t r = pi / np.rank_chunks;
-        const int64_t k = np.b0 * np.cps + (pi - r * np.rank_chunks);
-        const int64_t s = k / kNormSuper;
-        const int64_t first = s * kNormSuper;
-        const int64_t end = first + kNormSuper < np.cpr ? first + kNormSuper : np.cpr;
-        const int64_t launch_end = np.b0 * np.cps + np.rank_chunks;  // rank r's chunks here end
-        const int64_t stop = end < launch_end ? end : launch_end;
-        const int64_t seg_end = pi + (stop - k) < hi ? pi + (stop - k) : hi;
-        const int count = (int)(seg_end - pi);
-        const int size = (int)(end - first);
-        const bool whole = k == first && count == size;
-        for (int64_t q = pi; q < seg_end; ++q) {
-            FF x = chunk_fn(locate_chunk(np, q));
+    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x) {
+        const ChunkLoc L = locate_chunk(np, pi);
+        FF x = chunk_fn(L);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const FF y{__shfl_xor_sync(0xFFFFFFFFu, x.hi, o),
-                           __shfl_xor_sync(0xFFFFFFFFu, x.lo, o)};
-                x = ff_add(x, y);
-            }
-            if (lane == 0)
-                sh.wsum[buf][k - first + (q - pi)][warp] = x;
+        for (int o = 16; o > 0; o >>= 1) {
+            const FF y{__shfl_xor_sync(0xFFFFFFFFu, x.hi, o),
+                       __shfl_xor_sync(0xFFFFFFFFu, x.lo, o)};
+            x = ff_add(x, y);
         }
-        __syncthreads();
-        if (warp == 0) {
-            const int64_t ci0 = r * np.cpr + k;  // the segment's first chunk sum slot
-            for (int j = lane; j < count; j += 32) {
-                const int slot = (int)(k - first) + j;
-                FF t = sh.wsum[buf][slot][0];
-#pragma unroll
-                for (int w = 1; w < kThreads / 32; ++w)
-                    t = ff_add(t, sh.wsum[buf][slot][w]);
-                const double d = __dadd_rn((double)t.hi, (double)t.lo);
-                if (whole)
-                    sh.cp[slot] = d;
-                else
-                    np.partials[ci0 + j] = d;
-            }
-            __syncwarp();
-            const int64_t sci = r * np.spr + s;
-            if (whole) {
-                const double x = warp_fixed_sum_shared(sh.cp, size);
-                if (lane == 0) {
-                    np.sc_partials[sci] = x;
-                    sh.done_local += 1;
-                }
-            } else {
-                __threadfence();  // this lane's chunk sums before the count
-                __syncwarp();
-                int complete = 0;
-                if (lane == 0)
-                    complete = atomicAdd(&np.sc_count[sci], (uint32_t)count) + (uint32_t)count ==
-                               (uint32_t)size;
-                if (__shfl_sync(0xFFFFFFFFu, complete, 0))
-                    finish_superchunk(np, sci, r * np.cpr + first, size, sh);
-            }
-        }
-        pi = seg_end;
+        if (lane == 0)
+            np.leaves[L.ci * kNormLeaves + warp] = make_float2(x.hi, x.lo);
     }
-    if (warp == 0) {
-        __syncwarp();
-        if (lane == 0 && sh.done_local) {
-            __threadfence();  // the superchunk sums before their count
-            const uint32_t all = (uint32_t)((int64_t)np.ranks * np.spr);
-            if (atomicAdd(np.done, sh.done_local) + sh.done_local == all)
-                sh.final_pending = 1;
-        }
-    }
-    __syncthreads();
-    norm_finish(np, sh);
 }
 
 // Report a non-finite gradient of this warp once.

@@ -1,6 +1,7 @@
 // The streaming kernels of the step and the entry points zero_step_fused,
 // zero_step_fused_accumulated, zero_step_fused_buckets,
-// zero_reduce_scatter_sum and zero_reduce_scatter_accumulate.
+// zero_step_buckets_pass1 / _norm / _pass2, zero_reduce_scatter_sum and
+// zero_reduce_scatter_accumulate.
 //
 // One kernel template covers the passes over the data.  Each thread handles
 // 8-element units (16-byte loads of each rank's half gradient, 32-byte loads
@@ -10,10 +11,10 @@
 //   FUSED      (a2)-(a7) in one pass: reduce, unscale, flag, Adam from slot
 //              cur into slot 1 - cur, cast into the parameter buffer.
 //   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, the
-//              sum of squares over the norm's fixed tree (internal.h: chunks
-//              of the layout, not of the grid; the launch that completes the
-//              tree writes the total to the workspace), optionally keep g in
-//              a staging buffer.
+//              leaves of the norm's fixed tree (internal.h: chunks of the
+//              layout, not of the grid; the tree kernel then forms the
+//              total in the workspace), optionally keep g in a staging
+//              buffer.
 //   PASS2_*    (a5 clip)-(a7) of a clipped step, skipped when pass 1 flagged
 //              an overflow; it reads the total pass 1 formed; g is reduced
 //              again or read from the stage.  It walks the units backwards,
@@ -94,8 +95,8 @@ struct StepParams {
 };
 
 // A first pass's walk over its chunks of the norm's tree: each chunk's units
-// go through `unit` (which adds their squares to ss), then the chunk's sum
-// enters the tree (norm_walk in kernels.cuh).
+// go through `unit` (which adds their squares to ss), then the warps store
+// their leaves (norm_walk in kernels.cuh).
 template <bool ALL, class UnitFn>
 __device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, SumSq &ss,
                                           UnitFn &unit)
@@ -635,16 +636,14 @@ int check_slots(const zero_layout *layout, const zero_adam_cfg *cfg, float *cons
 }
 
 // The norm's tree for launches over buckets [b0, b0 + nbl) of `L` (the whole
-// layout), in workspace ws.  The counters are laid out for every rank of the
-// layout whatever the view, so a workspace serves every view of its layout.
+// layout), in workspace ws.
 NormPlan layout_plan(const zero_layout &L, int rank, int64_t b0, int64_t nbl, void *ws)
 {
     const bool bucketed = L.bucket_numel > 0;
     const int64_t nb = bucketed ? L.num_buckets : 1;
     const int64_t su = (bucketed ? L.slice_numel : L.owned_numel) / kUnit;
     const int64_t lsu = L.last_slice_numel / kUnit;
-    const NormGeom g = norm_geometry(su, lsu, nb);
-    return norm_plan(g, su, lsu, nb, b0, nbl, rank < 0 ? L.world : 1, (int64_t)L.world * g.spr,
+    return norm_plan(norm_geometry(su, lsu, nb), su, lsu, nb, b0, nbl, rank < 0 ? L.world : 1,
                      ws, nullptr);
 }
 
@@ -767,8 +766,8 @@ constexpr int64_t kKeepBytes = (int64_t)ZS_KEEP_MB << 20;
 // One whole step (one or two passes) in the given modes on a.lay.  The step's
 // last launch also ends the step (a8: its last CTA commits or skips); an empty
 // vector runs no pass and ends the step with the one-thread kernel.  A clipped
-// step's first pass forms the norm's tree in ws and the second pass reads its
-// total.
+// step's first pass stores the norm's leaves in ws, the tree kernel sums them
+// and the second pass reads the total.
 int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, void *ws,
              cudaStream_t stream)
 {
@@ -795,6 +794,8 @@ int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, void *w
     a.norm_total = norm_total_slot(ws);
     a.end_step = false;
     if ((rc = run(a, pass1, stream, &gx)))
+        return rc;
+    if ((rc = launch_norm_tree(a.norm, stream)))
         return rc;
     a.end_step = true;
     return run(a, pass2, stream, &gx);
@@ -1100,6 +1101,23 @@ extern "C" int zero_step_buckets_pass1(const void *const *grads, int grads_are_s
     a.norm = layout_plan(L, rank, first_bucket, n_buckets, ws);
     int gx;
     return run(a, M_PASS1, stream, &gx);
+}
+
+extern "C" int zero_step_buckets_norm(const zero_layout *layout, int rank, void *ws,
+                                     size_t ws_bytes, zero_stream_t stream)
+{
+    int rc = check_layout(layout);
+    if (rc)
+        return rc;
+    if (rank < -1 || rank >= layout->world)
+        return ZERO_EINVAL;
+    if ((rc = check_ws(layout, ws, ws_bytes)))
+        return rc;
+    const zero_layout &L = *layout;
+    if (L.padded_numel == 0)
+        return ZERO_OK;
+    return launch_norm_tree(layout_plan(L, rank, 0, L.bucket_numel ? L.num_buckets : 1, ws),
+                            stream);
 }
 
 extern "C" int zero_step_buckets_pass2(const void *const *grads, int grads_are_slices,
