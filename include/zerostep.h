@@ -213,12 +213,12 @@ ZERO_API int zero_state_init(zero_step_state *host_state, float loss_scale);
  * Bytes of device workspace a step on `layout` needs (zero_step_fused,
  * zero_step_fused_accumulated, zero_step_buckets_pass1 / _pass2), or, with
  * layout = NULL, the bytes zero_grad_norm needs for a vector of any length
- * (2,101,504).  0 for an invalid layout.
+ * (266,496).  0 for an invalid layout.
  * The workspace holds the tree over which the global sum of squares is
  * formed: chunks of at least 4096 elements of one rank's slice of one bucket
- * (about 32768 chunks per rank for large partitions), each summed as 8 warp
- * leaves; 64 chunks to a superchunk; then ranks.  It takes about 64 bytes per
- * chunk (16 MB for 8 billion parameters over 8 ranks).  Its shape depends
+ * (about 32768 chunks per rank for large partitions), 64 chunks to a
+ * superchunk, then ranks.  It takes about 8 bytes per chunk (2.1 MB for 8
+ * billion parameters over 8 ranks).  Its shape depends
  * only on the layout, so the sum's bits do not depend on the GPU, the grid,
  * or how the buckets are split into ranges.  ZERO-FILL THE WORKSPACE ONCE
  * before its first use: it holds one counter, which every call that runs to
@@ -287,7 +287,7 @@ ZERO_API int zero_check_overflow(const float *g, int64_t n, float inv_scale, int
  * Relative error about 1e-13 or better.  g: device, 32-byte aligned;
  * sumsq_dev: device double; ws: device workspace of ws_bytes >=
  * zero_workspace_bytes(NULL), zero-filled before its first use (the call
- * leaves its counter at zero).  Two launches: the leaves, then the tree (a
+ * leaves its counter at zero).  Two launches: the chunk sums, then the tree (a
  * memset for n = 0: *sumsq_dev = +0).
  * Pages: "zero-optimizer", "一. 优化前" (gradient-norm computation over fused
  * buffers); the clip rule itself is a reading (see zero_adam_cfg).
@@ -343,7 +343,7 @@ ZERO_API int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
  *  Result, arguments and summation order: as zero_grad_norm (the same kernel
  *  and the same tree, so the same bits), without ws / ws_bytes.
  *  Scratch: the tree lives in a library-owned static device array of
- *  ZERO_NOALLOC_SCRATCH_BYTES (2,101,504 bytes: the tree of a vector of any
+ *  ZERO_NOALLOC_SCRATCH_BYTES (266,496 bytes: the tree of a vector of any
  *  length) that every GPU which loads the library holds until the process
  *  exits.  A vector whose tree would not fit is rejected with ZERO_ESPACE
  *  (none is: the chunks grow with the vector).  The array's one counter is
@@ -355,7 +355,7 @@ ZERO_API int zero_step_fused_accumulated(const float *acc, zero_dtype dtype,
  *  address for the current device (cudaGetSymbolAddress) and caches it; make
  *  that first call before any stream capture.
  */
-#define ZERO_NOALLOC_SCRATCH_BYTES 2101504
+#define ZERO_NOALLOC_SCRATCH_BYTES 266496
 ZERO_API int zero_grad_norm_noalloc(const float *g, int64_t n, float inv_scale, double *sumsq_dev,
                                     zero_stream_t stream);
 
@@ -472,13 +472,13 @@ ZERO_API int zero_step_fused_buckets(const void *const *grads, int grads_are_sli
  *   1. zero_step_buckets_pass1 on every bucket of the layout, exactly once,
  *      in ranges [first_bucket, first_bucket + n_buckets): (a2) reduce, (a3)
  *      unscale, (a4) flag NaN/Inf in state_dev->found_inf, (a5) the squares'
- *      leaves into the workspace's fixed tree, and, with g_stage, keep the
+ *      chunk sums into the workspace's fixed tree, and, with g_stage, keep the
  *      unscaled gradient there.  A range can run as soon as its buckets'
  *      gradients are ready (during the backward pass), and ranges may run
  *      concurrently on different streams.
  *   2. zero_step_buckets_norm once, on a stream ordered after EVERY pass-1
- *      range: the tree above the leaves in its fixed order (chunks,
- *      superchunks, each rank, then the ranks in ascending order) gives the
+ *      range: the tree above the chunk sums in its fixed order
+ *      (superchunks, each rank, then the ranks in ascending order) gives the
  *      global sum of squares, kept in the workspace.
  *   3. zero_step_buckets_pass2 on every bucket, exactly once, in ranges, each
  *      on a stream ordered after step 2: (a5) the clip with c = min(1,
@@ -505,7 +505,7 @@ ZERO_API int zero_step_fused_buckets(const void *const *grads, int grads_are_sli
  *  master/m/v/params (pass 2): ping-pong slots as zero_step_fused; they may
  *    alias (in place), and must be device memory.
  * Every bucket must go through each pass exactly once per step; a bucket left
- * out of pass 1 leaves stale leaves in the tree.
+ * out of pass 1 leaves stale chunk sums in the tree.
  */
 ZERO_API int zero_step_buckets_pass1(const void *const *grads, int grads_are_slices,
                                      zero_dtype dtype, const zero_layout *layout, int rank,

@@ -15,7 +15,7 @@ EALIGN = -2
 ESPACE = -3
 ECUDA_BASE = -1000
 MAX_WORLD = 1024
-NOALLOC_SCRATCH_BYTES = 2101504
+NOALLOC_SCRATCH_BYTES = 266496
 
 
 class Layout(ctypes.Structure):

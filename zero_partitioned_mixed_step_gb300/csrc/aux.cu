@@ -131,12 +131,12 @@ __global__ void __launch_bounds__(kThreads)
     flag_nonfinite(bad, flag);
 }
 
-// The tree above the leaves that a first pass (or the first passes of all
-// the bucket ranges of a step) stored: every warp sums superchunks (lane l
-// takes chunks l and l + 32 of the superchunk, each the sum of its leaves in
-// warp order, then a fixed butterfly); the CTA that finishes last adds each
-// rank's superchunks (the same lane order) and then the ranks in ascending
-// order from +0, writes the total and returns the counter to zero.
+// The tree above the chunk sums that a first pass (or the first passes of
+// all the bucket ranges of a step) stored: every warp sums superchunks (lane
+// l adds chunks l and l + 32 of the superchunk from +0, then a fixed
+// butterfly); the CTA that finishes last adds each rank's superchunks (the
+// same lane order) and then the ranks in ascending order from +0, writes the
+// total and returns the counter to zero.
 __global__ void __launch_bounds__(kThreads) norm_tree_kernel(NormPlan np)
 {
     __shared__ double rank_sum[ZERO_MAX_WORLD];
@@ -146,25 +146,9 @@ __global__ void __launch_bounds__(kThreads) norm_tree_kernel(NormPlan np)
     const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
     for (int64_t sc = (int64_t)blockIdx.x * (kThreads / 32) + warp; sc < nsc; sc += warps) {
         const int64_t r = sc / np.spr, s = sc - r * np.spr;
-        const int64_t c0 = r * np.cpr + s * kNormSuper;
         const int64_t left = np.cpr - s * kNormSuper;
-        const int64_t size = left < kNormSuper ? left : kNormSuper;
-        double x = 0.0;
-        for (int64_t j = lane; j < size; j += 32) {
-            const float2 *lf = np.leaves + (c0 + j) * kNormLeaves;
-            float2 v[kNormLeaves];
-#pragma unroll
-            for (int w = 0; w < kNormLeaves; ++w)
-                v[w] = __ldcg(lf + w);
-            FF t{v[0].x, v[0].y};
-#pragma unroll
-            for (int w = 1; w < kNormLeaves; ++w)
-                t = ff_add(t, FF{v[w].x, v[w].y});
-            x = __dadd_rn(x, __dadd_rn((double)t.hi, (double)t.lo));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+        const double x = warp_fixed_sum(np.partials + r * np.cpr + s * kNormSuper,
+                                        left < kNormSuper ? left : kNormSuper);
         if (lane == 0)
             np.sc_partials[sc] = x;
     }
@@ -202,8 +186,8 @@ int launch_norm_tree(const NormPlan &np, cudaStream_t stream)
     return e == cudaSuccess ? ZERO_OK : cuda_error(e);
 }
 
-// The leaves of the sum of squares of g * inv_s, the vector taken as one
-// rank's single slice of ceil(n / 8) units (the last one padded with zeros).
+// The chunk sums of the squares of g * inv_s, the vector taken as one rank's
+// single slice of ceil(n / 8) units (the last one padded with zeros).
 __global__ void __launch_bounds__(kThreads)
     norm_kernel(const float *g, int64_t n, float inv_s, NormPlan np)
 {
@@ -229,7 +213,7 @@ __global__ void __launch_bounds__(kThreads)
     });
 }
 
-// zero_grad_norm's two launches (the leaves, then the tree) with the tree in
+// zero_grad_norm's two launches (the chunk sums, then the tree) with the tree in
 // `ws`, a workspace of ws_bytes bytes whose counter is zero.
 static int launch_norm(const float *g, int64_t n, float inv_scale, double *sumsq_dev, void *ws,
                        size_t ws_bytes, cudaStream_t stream)
@@ -390,7 +374,7 @@ static_assert(kNormWsAnyVector == ZERO_NOALLOC_SCRATCH_BYTES,
               "the static scratch holds the tree of any vector");
 
 // The tree of one call: its counter (zero when the library is loaded, and
-// returned to zero by every call that completes), leaves and superchunk sums.  Every GPU that loads the library holds this array
+// returned to zero by every call that completes), chunk and superchunk sums.  Every GPU that loads the library holds this array
 // until the process exits.  In host code the name is only a host-side
 // stand-in for the device array: kernels must be given the address
 // cudaGetSymbolAddress returns for the current device.

@@ -53,8 +53,7 @@ NormGeom norm_geometry(int64_t slice_units, int64_t last_slice_units, int64_t nb
 
 size_t norm_ws_bytes(int64_t ranks, const NormGeom &g)
 {
-    return (size_t)(kWsHeader + ranks * g.cpr * kNormLeaves * (int64_t)sizeof(float2) +
-                    ranks * g.spr * (int64_t)sizeof(double));
+    return (size_t)(kWsHeader + ranks * (g.cpr + g.spr) * (int64_t)sizeof(double));
 }
 
 NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_units, int64_t nb,
@@ -77,8 +76,8 @@ NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_un
     p.ranks = ranks;
     char *base = static_cast<char *>(ws);
     p.done = reinterpret_cast<uint32_t *>(base);
-    p.leaves = reinterpret_cast<float2 *>(base + kWsHeader);
-    p.sc_partials = reinterpret_cast<double *>(p.leaves + (int64_t)ranks * g.cpr * kNormLeaves);
+    p.partials = reinterpret_cast<double *>(base + kWsHeader);
+    p.sc_partials = p.partials + (int64_t)ranks * g.cpr;
     p.total = total ? total : norm_total_slot(ws);
     return p;
 }

@@ -28,24 +28,22 @@ int check_cfg(const zero_adam_cfg *cfg);
 // The global sum of squares is formed over a tree whose shape depends only on
 // the layout (never on the device or the grid), so every launch shape, every
 // split of the buckets into ranges and every GPU give the same bits:
-//   leaf       one warp's share of a chunk: a chunk is kNormChunkMinUnits ..
-//              units of one rank's slice of one bucket (chunks restart at
-//              every slice boundary), summed by one CTA: thread t takes units
-//              t, t + 256, ...; each warp adds its lanes with a fixed
-//              butterfly and stores the pair;
-//   chunk      its 8 leaves in warp order;
+//   chunk      kNormChunkMinUnits .. units of one rank's slice of one bucket
+//              (chunks restart at every slice boundary), summed by one CTA:
+//              thread t takes units t, t + 256, ...; each warp adds its
+//              lanes with a fixed butterfly, then the 8 warps' pairs are
+//              added in warp order and the pair rounded to binary64;
 //   superchunk kNormSuper consecutive chunks of one rank, in a fixed lane
 //              order;
 //   rank       its superchunks in a fixed lane order;
 //   total      the ranks' sums added in ascending rank order from +0.
-// The first pass stores leaves only (no synchronisation between CTAs); the
-// tree kernel (launch_norm_tree) forms the rest.  One rank's view forms its
+// The first pass stores the chunk sums only (no synchronisation between
+// CTAs); the tree kernel (launch_norm_tree) forms the rest.  One rank's view forms its
 // own rank sum only; an every-rank launch gives exactly the rank-order sum of
 // the per-rank results.
 constexpr int64_t kNormChunkMinUnits = 512;      // 4096 elements
 constexpr int64_t kNormChunksPerRank = 32768;    // target upper bound per rank
 constexpr int kNormSuper = 64;                   // chunks per superchunk
-constexpr int kNormLeaves = kThreads / 32;       // leaves (warps) per chunk
 
 // Chunk geometry of one rank's elements.
 struct NormGeom {
@@ -73,7 +71,7 @@ struct NormPlan {
     int32_t ranks;          // ranks whose sums are formed (world, or 1 for one rank's view)
     int32_t pad_;
     uint32_t *done;         // the tree kernel's finished CTAs (zero between launches)
-    float2 *leaves;         // kNormLeaves (hi, lo) pairs per chunk
+    double *partials;       // chunk sums
     double *sc_partials;    // superchunk sums
     double *total;          // where the total goes
 };
@@ -88,7 +86,7 @@ NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_un
                    int64_t b0, int64_t nbl, int32_t ranks, void *ws, double *total);
 // Bytes zero_grad_norm needs for a vector of any length (one rank, one slice:
 // at most kNormChunksPerRank chunks, as the chunk grows with the vector).
-constexpr size_t kNormWsAnyVector = kWsHeader + kNormChunksPerRank * kNormLeaves * 8 +
+constexpr size_t kNormWsAnyVector = kWsHeader + kNormChunksPerRank * 8 +
                                     (kNormChunksPerRank / kNormSuper) * 8;
 inline size_t norm_ws_bytes_any_vector() { return kNormWsAnyVector; }
 // The workspace's result slot (written by the tree kernel).
@@ -96,7 +94,7 @@ inline double *norm_total_slot(void *ws)
 {
     return reinterpret_cast<double *>(static_cast<char *>(ws) + 8);
 }
-// The tree kernel: leaves -> chunks -> superchunks -> ranks -> total (aux.cu).
+// The tree kernel: chunks -> superchunks -> ranks -> total (aux.cu).
 int launch_norm_tree(const NormPlan &np, struct CUstream_st *stream);
 
 }  // namespace zs

@@ -568,14 +568,18 @@ __device__ __forceinline__ double warp_fixed_sum(const double *p, int64_t n)
 
 // ------------------------------------------------------------------ the norm's tree
 //
-// Leaves, chunks, superchunks, ranks (see NormPlan in internal.h).  A first
-// pass walks its chunks with a grid stride, so that at any moment the CTAs
-// stream neighbouring memory (every-rank launches take the chunks bucket by
-// bucket and rank by rank inside a bucket: the flat order); a whole CTA sums
-// one chunk, and each warp stores its leaf.  Nothing in the walk waits for
-// another warp or CTA.
+// Chunks, superchunks, ranks (see NormPlan in internal.h).  A first pass
+// walks its chunks with a grid stride, so that at any moment the CTAs stream
+// neighbouring memory (every-rank launches take the chunks bucket by bucket
+// and rank by rank inside a bucket: the flat order); a whole CTA sums one
+// chunk, and a barrier per chunk keeps the CTA's warps on the same chunk:
+// each of its 256-unit rows is then read by all 8 warps at once (4 KB of
+// each gradient, 8 KB of each fp32 array), which measured 10 % faster on an
+// 8-billion-element first pass than letting the warps drift apart.  After
+// the barrier warp 0 adds the warps' pairs and stores the chunk's sum.
+// Nothing waits for another CTA.
 
-// Where a chunk lies and where its leaves go.
+// Where a chunk lies and where its sum goes.
 struct ChunkLoc {
     int64_t r;        // rank, relative to the launch (0 for one rank's view)
     int64_t bl;       // bucket, relative to the launch
@@ -617,8 +621,10 @@ __device__ __forceinline__ ChunkLoc locate_chunk(const NormPlan &np, int64_t pi)
 template <class ChunkFn>
 __device__ __forceinline__ void norm_walk(const NormPlan &np, ChunkFn &&chunk_fn)
 {
+    __shared__ FF warp_sum[2][kThreads / 32];  // double-buffered by chunk parity
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x) {
+    int parity = 0;
+    for (int64_t pi = blockIdx.x; pi < np.launch_chunks; pi += gridDim.x, parity ^= 1) {
         const ChunkLoc L = locate_chunk(np, pi);
         FF x = chunk_fn(L);
 #pragma unroll
@@ -628,7 +634,15 @@ __device__ __forceinline__ void norm_walk(const NormPlan &np, ChunkFn &&chunk_fn
             x = ff_add(x, y);
         }
         if (lane == 0)
-            np.leaves[L.ci * kNormLeaves + warp] = make_float2(x.hi, x.lo);
+            warp_sum[parity][warp] = x;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            FF t = warp_sum[parity][0];
+#pragma unroll
+            for (int w = 1; w < kThreads / 32; ++w)
+                t = ff_add(t, warp_sum[parity][w]);
+            np.partials[L.ci] = __dadd_rn((double)t.hi, (double)t.lo);
+        }
     }
 }
 

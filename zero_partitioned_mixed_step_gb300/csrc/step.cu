@@ -11,7 +11,7 @@
 //   FUSED      (a2)-(a7) in one pass: reduce, unscale, flag, Adam from slot
 //              cur into slot 1 - cur, cast into the parameter buffer.
 //   PASS1      (a2)-(a5) of a clipped step: reduce, unscale, flag, the
-//              leaves of the norm's fixed tree (internal.h: chunks of the
+//              chunk sums of the norm's fixed tree (internal.h: chunks of the
 //              layout, not of the grid; the tree kernel then forms the
 //              total in the workspace), optionally keep g in a staging
 //              buffer.
@@ -95,8 +95,8 @@ struct StepParams {
 };
 
 // A first pass's walk over its chunks of the norm's tree: each chunk's units
-// go through `unit` (which adds their squares to ss), then the warps store
-// their leaves (norm_walk in kernels.cuh).
+// go through `unit` (which adds their squares to ss), then the chunk's sum is
+// stored (norm_walk in kernels.cuh).
 template <bool ALL, class UnitFn>
 __device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, SumSq &ss,
                                           UnitFn &unit)
@@ -327,6 +327,12 @@ __global__ void __launch_bounds__(kThreads, 5)
 
 // ------------------------------------------------------------------ launch
 
+// CTAs per SM of a first pass at most (when more fit).  Swept on the 8B
+// clipped step (bf16, 8 ranks) and the 124M one, same box: 3 per SM 61.95 /
+// 0.988 ms, 4 per SM 61.16 / 0.963 ms, 5 per SM 61.23 / 0.949 ms, all that fit
+// (6) 61.64 / 0.947 ms.
+constexpr int kFirstPassCtasPerSm = 5;
+
 template <int DT, int W, int MAXW, int MODE, bool HOST_STATE = false>
 int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
 {
@@ -337,7 +343,9 @@ int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
     else
         kern = p.view.all_ranks ? step_kernel<DT, W, MAXW, MODE, true>
                                 : step_kernel<DT, W, MAXW, MODE, false>;
-    const int target = target_ctas(reinterpret_cast<const void *>(kern));
+    int target = target_ctas(reinterpret_cast<const void *>(kern));
+    if (sums_squares(MODE) && target > device_sms() * kFirstPassCtasPerSm)
+        target = device_sms() * kFirstPassCtasPerSm;
     const int64_t want = sums_squares(MODE) ? p.norm.launch_chunks
                                             : (p.view.units + kThreads - 1) / kThreads;
     const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
@@ -766,8 +774,8 @@ constexpr int64_t kKeepBytes = (int64_t)ZS_KEEP_MB << 20;
 // One whole step (one or two passes) in the given modes on a.lay.  The step's
 // last launch also ends the step (a8: its last CTA commits or skips); an empty
 // vector runs no pass and ends the step with the one-thread kernel.  A clipped
-// step's first pass stores the norm's leaves in ws, the tree kernel sums them
-// and the second pass reads the total.
+// step's first pass stores the norm's chunk sums in ws, the tree kernel sums
+// them and the second pass reads the total.
 int run_step(PassArgs &a, bool clip, int one_pass, int pass1, int pass2, void *ws,
              cudaStream_t stream)
 {
