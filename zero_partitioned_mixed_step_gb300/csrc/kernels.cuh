@@ -53,12 +53,36 @@ __device__ __forceinline__ uint4 ld_stream(const uint16_t *p, uint64_t pol)
     return r;
 }
 
+// ld_stream issued where it is written (not moved past a later barrier).
+__device__ __forceinline__ uint4 ld_stream_now(const uint16_t *p, uint64_t pol)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
 // 8 fp32 values (32 bytes, 32-byte aligned) in one 256-bit access.  The
 // coherent path is used because a clipped step may update the state in place.
 __device__ __forceinline__ void load8(const float *p, float x[8])
 {
     uint32_t u[8];
     asm("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7])
+        : "l"(p));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        x[i] = __uint_as_float(u[i]);
+}
+
+// load8 issued where it is written (not moved past a later barrier).
+__device__ __forceinline__ void load8_now(const float *p, float x[8])
+{
+    uint32_t u[8];
+    asm volatile(
+        "ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
         : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
           "=r"(u[7])
         : "l"(p));
@@ -430,26 +454,29 @@ __device__ __forceinline__ void end_step(const FinCfg &c, zero_step_state *st, i
     st->found_inf = 0;
 }
 
-// The end of the step's last kernel, called by every thread of every CTA:
-// the step is ended by the CTA that finishes last, so no separate launch is
-// needed.  Bit 0 of found_inf is the step's non-finite flag; while the kernel
-// runs, the bits above count its CTAs that are done (found_inf is 0 between
-// steps, and end_step clears it).  A CTA's flag updates come before its count
-// (barrier, then a fence), and all updates are atomics on the one word, so
-// the CTA whose addition completes the count sees every CTA's flag in the old
-// value; all CTAs read the state they need when they start, before they
-// count themselves.
-__device__ __forceinline__ void arrive_and_end_step(const FinCfg &c, zero_step_state *st)
+// The end of a kernel, called by every thread of every CTA: OR the CTA's
+// non-finite flag into bit 0 of found_inf and, when the launch is the step's
+// last, count the CTA in the bits above; the CTA whose count completes the
+// grid ends the step (commit or skip, a8), so no separate launch is needed.
+// One thread does both atomics, the OR first: one thread's atomics on one
+// word stay in order, so the count the last CTA sees carries every CTA's
+// flag, and no fence is needed (what the step wrote reaches the next kernel
+// through the kernel boundary).  found_inf is 0 between steps (end_step
+// clears it), and every CTA reads the state it needs when it starts, before
+// it counts itself, so the commit never races a reader.
+__device__ __forceinline__ void finish_cta(bool bad, bool ends, const FinCfg &c,
+                                           zero_step_state *st)
 {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const int32_t old = atomicAdd(&st->found_inf, 2);
-        if ((old >> 1) == (int32_t)gridDim.x - 1) {
-            __threadfence();
-            end_step(c, st, 1, old & 1);
-        }
-    }
+    const int any = __syncthreads_or(bad ? 1 : 0);
+    if (threadIdx.x != 0)
+        return;
+    if (any)
+        atomicOr(&st->found_inf, 1);
+    if (!ends)
+        return;
+    const int32_t old = atomicAdd(&st->found_inf, 2);
+    if ((old >> 1) == (int32_t)gridDim.x - 1)
+        end_step(c, st, 1, old & 1);
 }
 
 // ------------------------------------------------------------------ Adam

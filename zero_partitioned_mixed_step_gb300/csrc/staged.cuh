@@ -237,11 +237,8 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
                         break;
             }
         }
-    } else {
-        flag_nonfinite(bad, &p.state->found_inf);
     }
-    if (p.end_step)
-        arrive_and_end_step(p.fin, p.state);
+    finish_cta(abort_flag || bad, p.end_step != 0, p.fin, p.state);
 }
 
 }  // namespace zs

@@ -131,6 +131,32 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     int cur = 0;
     const View &vw = p.view;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const uint64_t pol = evict_first_policy();
+    // One-pass steps over at most 4 ranks issue their first unit's loads
+    // before the prologue's barrier (the gradients need nothing, the state
+    // only the slot index), so that they are in flight while thread 0 forms
+    // the step's scalars.  (At 8 and 16 ranks the loads held across the
+    // barrier took ptxas from 78 and 71 registers to 90 and 119, a CTA per SM
+    // fewer; at 2 ranks it went from 78 to 64, a CTA per SM more.)
+    constexpr bool kEarly = MODE == M_FUSED && !HOST_STATE && W > 0 && W <= 4 &&
+                            !half_reduce(DT);
+    const int64_t u_first = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    uint4 early_g[kEarly ? W : 1];
+    float early_w[8], early_m[8], early_v[8];
+    int64_t early_f = 0, early_si = 0;
+    if constexpr (kEarly) {
+        if (u_first < vw.units) {
+            int64_t gi;
+            locate<ALL>(vw, u_first, early_f, early_si, gi);
+            const int c0 = p.state->cur;
+            load8_now((c0 ? p.w1 : p.w0) + early_si, early_w);
+            load8_now((c0 ? p.m1 : p.m0) + early_si, early_m);
+            load8_now((c0 ? p.v1 : p.v0) + early_si, early_v);
+#pragma unroll
+            for (int q = 0; q < W; ++q)
+                early_g[q] = ld_stream_now(p.grads.p[q] + gi, pol);
+        }
+    }
     if constexpr (!reduces_only(MODE)) {
         if constexpr (second_pass(MODE)) {
             // The global sum of squares the first pass formed; CTA 0
@@ -173,7 +199,6 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     float *v_dst = cur ? p.vo0 : p.vo1;
     uint16_t *out = cur ? p.par0 : p.par1;
 
-    const uint64_t pol = evict_first_policy();
     uint64_t keep_pol = pol;
     if constexpr (sums_squares(MODE))
         keep_pol = evict_last_policy();
@@ -291,15 +316,34 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
             }
         }
     } else {
-        for (int64_t u = base + threadIdx.x; u < vw.units; u += stride)
+        int64_t u = base + threadIdx.x;
+        if constexpr (kEarly) {
+            if (u < vw.units) {  // the unit whose loads were issued before the barrier
+                float g[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    g[i] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < W; ++q)
+                    add_half8<DT>(g, early_g[q]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    g[i] = __fmul_rn(g[i], s.inv_s);
+                    bad |= nonfinite(g[i]);
+                }
+                adam8(g, early_w, early_m, early_v, s);
+                store8(w_dst + early_si, early_w);
+                store8(m_dst + early_si, early_m);
+                store8(v_dst + early_si, early_v);
+                st_half8(out + early_f, pack_half8<DT>(early_w), pol);
+            }
+            u += stride;
+        }
+        for (; u < vw.units; u += stride)
             unit(u);
     }
-    if constexpr (flags_overflow(MODE))
-        flag_nonfinite(bad, &p.state->found_inf);
-    if constexpr (ends_step(MODE)) {
-        if (p.end_step)
-            arrive_and_end_step(p.fin, p.state);
-    }
+    if constexpr (flags_overflow(MODE) || ends_step(MODE))
+        finish_cta(bad, ends_step(MODE) && p.end_step, p.fin, p.state);
 }
 
 // Device-resident state: the launch bound names only the block size, and
