@@ -534,8 +534,8 @@ def run_e2e(z, grads, wl, args, steps: int = 20):
     """End to end through ZeroStep.step_from_host: every rank's gradient sits
     in page-locked host memory (the library's zero_host_alloc blocks) and the
     step's kernels load it over the host link (zero-copy: every step moves
-    the gradients host -> device inside the timed region; with offloaded
-    state they are copied in first), then the step state is read back to the
+    the gradients host -> device inside the timed region), then the step
+    state is read back to the
     host; each of `steps` steps is timed on its own with the host clock (the
     call returns after the state has reached the host).  The value is the
     median step's rate; min and max of the rate and the link rate of the same
@@ -551,9 +551,7 @@ def run_e2e(z, grads, wl, args, steps: int = 20):
     for h, g in zip(host, grads):
         h.copy_(g)
     stream = torch.cuda.current_stream()
-    # With the optimizer state offloaded too, the kernel's host traffic is the
-    # state's; the gradients are then copied in first by the copy engines.
-    dev = grads if wl.offload_state else None
+    dev = None  # the step's kernels load the gradients straight from host memory
     z.step_from_host(host, dev, stream, wl.micro_steps)  # warm-up
     torch.cuda.synchronize()
     times = []
@@ -570,8 +568,7 @@ def run_e2e(z, grads, wl, args, steps: int = 20):
             "min": params / max(times) / 1e9, "max": params / min(times) / 1e9,
             "link_gbs": h2d / med / 1e9, "link_gbs_min": h2d / max(times) / 1e9,
             "link_gbs_max": h2d / min(times) / 1e9,
-            "h2d": ("copied into device buffers, then the step" if wl.offload_state else
-                    "the step's kernels load the gradients from page-locked host memory")}
+            "h2d": "the step's kernels load the gradients from page-locked host memory"}
 
 
 def main():

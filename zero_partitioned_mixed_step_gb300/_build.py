@@ -28,7 +28,10 @@ def nvcc() -> str:
     if not os.path.exists(path):
         raise RuntimeError("nvcc not found (install the CUDA toolkit or set CUDA_HOME)")
     return path
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
+# -fmad=false keeps device arithmetic uncontracted; -ffp-contract=off does the
+# same for the host code (the host rounds configuration-only scalars).
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-ffp-contract=off",
+              "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-Wall", "-I", INCLUDE, *ARCH]
 
 

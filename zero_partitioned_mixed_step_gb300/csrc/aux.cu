@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kThreads)
                 CfgDev cfg, const zero_step_state *st)
 {
     __shared__ Scalars sh;
-    if (threadIdx.x == 0)
-        compute_scalars(cfg, st, st->sumsq, sh);
+    __shared__ int sh_cur;
+    form_scalars(cfg, st, &st->sumsq, sh, sh_cur);
     __syncthreads();
     const Scalars s = sh;
     if (s.skip)
@@ -334,8 +334,7 @@ int zero_adam_step(const float *g, float *master, float *m, float *v, void *half
         return ZERO_EALIGN;
     if (n == 0)
         return ZERO_OK;
-    const CfgDev c{cfg->lr, cfg->beta1, cfg->beta2, cfg->eps, cfg->weight_decay,
-                   cfg->max_grad_norm, cfg->adamw ? 1 : 0, cfg->bias_correction ? 1 : 0};
+    const CfgDev c = make_cfg_dev(*cfg);
     uint16_t *out = static_cast<uint16_t *>(half_out);
     if (!is_bf16(dtype)) {  // the output's storage type
         const int gx = grid_for(reinterpret_cast<const void *>(adam_kernel<ZERO_F16>), n / kUnit);

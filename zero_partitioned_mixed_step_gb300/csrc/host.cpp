@@ -82,6 +82,27 @@ NormPlan norm_plan(const NormGeom &g, int64_t slice_units, int64_t last_slice_un
     return p;
 }
 
+CfgDev make_cfg_dev(const zero_adam_cfg &c)
+{
+    CfgDev d{};
+    d.lr = c.lr;
+    d.beta1 = c.beta1;
+    d.beta2 = c.beta2;
+    d.max_norm = c.max_grad_norm;
+    d.b1 = (float)c.beta1;
+    d.omb1 = (float)(1.0 - c.beta1);
+    d.b2 = (float)c.beta2;
+    d.omb2 = (float)(1.0 - c.beta2);
+    d.eps = (float)c.eps;
+    const double lr_wd = c.lr * c.weight_decay;  // rounded on its own (no contraction)
+    d.decay = (float)(1.0 - lr_wd);
+    d.wd = (float)c.weight_decay;
+    d.lr_f = (float)c.lr;
+    d.adamw = c.adamw ? 1 : 0;
+    d.bias_correction = c.bias_correction ? 1 : 0;
+    return d;
+}
+
 static bool power_of_two(double x)
 {
     int e;

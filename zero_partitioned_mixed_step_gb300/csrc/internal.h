@@ -23,6 +23,18 @@ inline int cuda_error(int err) { return ZERO_ECUDA_BASE - err; }
 int check_layout(const zero_layout *lay);
 int check_cfg(const zero_adam_cfg *cfg);
 
+// The optimizer configuration as the kernels use it: the values the step
+// needs in binary64 (lr and the betas, for the bias corrections; the clip
+// threshold), and the values that depend on the configuration alone, formed
+// on the host in binary64 and rounded once to binary32 (the library's host
+// code is compiled without floating-point contraction).
+struct CfgDev {
+    double lr, beta1, beta2, max_norm;
+    float b1, omb1, b2, omb2, eps, decay, wd, lr_f;  // beta1, 1 - beta1, ..., 1 - lr wd, wd, lr
+    int32_t adamw, bias_correction;
+};
+CfgDev make_cfg_dev(const zero_adam_cfg &c);
+
 // ------------------------------------------------------------------ the norm's summation tree
 //
 // The global sum of squares is formed over a tree whose shape depends only on

@@ -365,11 +365,6 @@ __device__ __forceinline__ void locate(const View &v, int64_t u, int64_t &f, int
 
 // ------------------------------------------------------------------ per-step scalars
 
-struct CfgDev {
-    double lr, beta1, beta2, eps, wd, max_norm;
-    int32_t adamw, bias_correction;
-};
-
 struct Scalars {
     float inv_s, b1, omb1, b2, omb2, step, rbc2, eps, decay, wd, coef;
     int32_t adamw, clip, skip;
@@ -382,32 +377,43 @@ __device__ __forceinline__ float clip_coefficient(double sumsq, double max_norm)
     return __double2float_rn(fmin(1.0, __ddiv_rn(max_norm, __dadd_rn(__dsqrt_rn(sumsq), 1e-6))));
 }
 
-// Scalars of step t + 1 from the state at the start of the step; sumsq is the
-// step's global sum of squares (read only when clipping).
-__device__ __forceinline__ void compute_scalars(const CfgDev &c, const zero_step_state *st,
-                                                double sumsq, Scalars &s)
+// Scalars of step t + 1 from the state at the start of the step, formed by
+// three threads of different warps so that the binary64 division and square
+// roots (slow on GB300's binary64 pipe) run at the same time on different
+// sub-partitions: thread 0 reads the state's flags and forms step = lr /
+// (1 - beta1^t) (beta1^t = beta1_pow * beta1), thread 32 forms rbc2 =
+// sqrt(1 - beta2^t), thread 64 the clip coefficient when `total` (the step's
+// global sum of squares) is given.  The configuration-only values were rounded
+// on the host (make_cfg_dev).  A barrier must follow before sh is read; every
+// CTA has at least 96 threads.
+__device__ __forceinline__ void form_scalars(const CfgDev &c, const zero_step_state *st,
+                                             const double *total, Scalars &sh, int &sh_cur)
 {
-    const double bp1 = __dmul_rn(st->beta1_pow, c.beta1);
-    const double bp2 = __dmul_rn(st->beta2_pow, c.beta2);
-    if (c.bias_correction) {
-        s.step = __double2float_rn(__ddiv_rn(c.lr, __dsub_rn(1.0, bp1)));
-        s.rbc2 = __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, bp2)));
-    } else {
-        s.step = __double2float_rn(c.lr);
-        s.rbc2 = 1.0f;
+    if (threadIdx.x == 0) {
+        sh.b1 = c.b1;
+        sh.omb1 = c.omb1;
+        sh.b2 = c.b2;
+        sh.omb2 = c.omb2;
+        sh.eps = c.eps;
+        sh.decay = c.decay;
+        sh.wd = c.wd;
+        sh.adamw = c.adamw;
+        sh.clip = c.max_norm > 0.0;
+        sh.inv_s = __fdiv_rn(1.0f, st->loss_scale);
+        sh.skip = st->found_inf & 1;
+        sh_cur = st->cur;
+        sh.step = c.bias_correction
+                      ? __double2float_rn(__ddiv_rn(c.lr, __dsub_rn(1.0, __dmul_rn(st->beta1_pow,
+                                                                                   c.beta1))))
+                      : c.lr_f;
+    } else if (threadIdx.x == 32) {
+        sh.rbc2 = c.bias_correction
+                      ? __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, __dmul_rn(st->beta2_pow,
+                                                                              c.beta2))))
+                      : 1.0f;
+    } else if (threadIdx.x == 64) {
+        sh.coef = total && c.max_norm > 0.0 ? clip_coefficient(__ldcg(total), c.max_norm) : 1.0f;
     }
-    s.b1 = __double2float_rn(c.beta1);
-    s.omb1 = __double2float_rn(__dsub_rn(1.0, c.beta1));
-    s.b2 = __double2float_rn(c.beta2);
-    s.omb2 = __double2float_rn(__dsub_rn(1.0, c.beta2));
-    s.eps = __double2float_rn(c.eps);
-    s.decay = __double2float_rn(__dsub_rn(1.0, __dmul_rn(c.lr, c.wd)));
-    s.wd = __double2float_rn(c.wd);
-    s.adamw = c.adamw;
-    s.inv_s = __fdiv_rn(1.0f, st->loss_scale);
-    s.clip = c.max_norm > 0.0;
-    s.coef = s.clip ? clip_coefficient(sumsq, c.max_norm) : 1.0f;
-    s.skip = st->found_inf & 1;
 }
 
 // ------------------------------------------------------------------ end of step

@@ -108,9 +108,8 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
     constexpr int gbytes = W * kStagedTile * 2;
     const int nst = p.stages;
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
+    form_scalars(p.cfg, p.state, nullptr, sh, sh_cur);
     if (tid == 0) {
-        compute_scalars(p.cfg, p.state, p.state->sumsq, sh);
-        sh_cur = p.state->cur;
         abort_flag = 0;
         for (int st = 0; st < nst; ++st) {
             const uint32_t a = (uint32_t)__cvta_generic_to_shared(&full[st]);

@@ -91,6 +91,7 @@ struct StepParams {
     int32_t discard;
     // The step's last kernel: the CTA that finishes last ends the step (a8).
     int32_t end_step;
+    int32_t host_grads;  // the gradients are in page-locked host memory (host side only)
     FinCfg fin;
 };
 
@@ -158,25 +159,19 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
         }
     }
     if constexpr (!reduces_only(MODE)) {
-        if constexpr (second_pass(MODE)) {
-            // The global sum of squares the first pass formed; CTA 0
-            // publishes it in the state when the step is not skipped.
-            if (threadIdx.x == 0) {
-                const double total = __ldcg(p.norm_total);
-                compute_scalars(p.cfg, p.state, total, sh);
-                sh_cur = p.state->cur;
-                if (blockIdx.x == 0 && !sh.skip) {
-                    p.state->sumsq = total;
-                    p.state->clip_coef = sh.coef;
-                }
-            }
-        } else if (threadIdx.x == 0) {
-            compute_scalars(p.cfg, p.state, p.state->sumsq, sh);
-            sh_cur = p.state->cur;
-        }
+        // A second pass also forms the clip coefficient from the global sum
+        // of squares the first pass formed; CTA 0 publishes both in the state
+        // when the step is not skipped.
+        form_scalars(p.cfg, p.state, second_pass(MODE) ? p.norm_total : nullptr, sh, sh_cur);
         __syncthreads();
         s = sh;
         cur = sh_cur;
+        if constexpr (second_pass(MODE)) {
+            if (blockIdx.x == 0 && threadIdx.x == 0 && !s.skip) {
+                p.state->sumsq = __ldcg(p.norm_total);
+                p.state->clip_coef = s.coef;
+            }
+        }
     }
     bool work = true;
     if constexpr (second_pass(MODE)) {
@@ -361,7 +356,8 @@ __global__ void __launch_bounds__(kThreads)
 // per SM (at most 51 registers).  Host accesses take microseconds, so more
 // warps in flight pay: timed on the 1.5B, 16-rank offloaded step, 156 ms at 5
 // CTAs/SM against 174 ms at the natural 3 (225 ms at 4, 196 ms at 6: the
-// register caps also reorder the loads).
+// register caps also reorder the loads).  When the gradients are in host
+// memory too, the launch takes at most kHostAllCtasPerSm CTAs per SM.
 template <int DT, int W, int MAXW, int MODE, bool ALL>
 __global__ void __launch_bounds__(kThreads, 5)
     step_kernel_host_state(const __grid_constant__ StepParams<MAXW> p)
@@ -370,6 +366,13 @@ __global__ void __launch_bounds__(kThreads, 5)
 }
 
 // ------------------------------------------------------------------ launch
+
+// CTAs per SM at most when the state and the gradients are all in page-locked
+// host memory.  The 1.5B, 16-rank offloaded step with its gradients in host
+// memory, one box: 760 CTAs (5 per SM) 985 ms per step, the host link read at
+// 67 GB/s; 456 CTAs (3 per SM) and 152 CTAs 322 ms, 205 GB/s (the link's
+// rate).  Too many loads to host memory in flight collapse the link's rate.
+constexpr int kHostAllCtasPerSm = 3;
 
 // CTAs per SM of a first pass at most (when more fit).  Swept on the 8B
 // clipped step (bf16, 8 ranks) and the 124M one, same box: 3 per SM 61.95 /
@@ -390,6 +393,8 @@ int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
     int target = target_ctas(reinterpret_cast<const void *>(kern));
     if (sums_squares(MODE) && target > device_sms() * kFirstPassCtasPerSm)
         target = device_sms() * kFirstPassCtasPerSm;
+    if (HOST_STATE && p.host_grads && target > device_sms() * kHostAllCtasPerSm)
+        target = device_sms() * kHostAllCtasPerSm;
     const int64_t want = sums_squares(MODE) ? p.norm.launch_chunks
                                             : (p.view.units + kThreads - 1) / kThreads;
     const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
@@ -519,8 +524,7 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
     v.world = world;
     if (a.cfg) {
         const zero_adam_cfg &c = *a.cfg;
-        p.cfg = CfgDev{c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, c.max_grad_norm,
-                       c.adamw ? 1 : 0, c.bias_correction ? 1 : 0};
+        p.cfg = make_cfg_dev(c);
     }
     p.state = a.state;
     if (a.master) {
@@ -540,6 +544,7 @@ int run_pass(const PassArgs &a, int mode, cudaStream_t stream, int *gx)
     p.keep_from = a.keep_from < v.units ? a.keep_from : v.units;
     p.discard = a.discard && p.keep_from < v.units ? 1 : 0;
     p.end_step = a.end_step ? 1 : 0;
+    p.host_grads = a.grads && !a.grads_on_device ? 1 : 0;
     if (a.cfg)
         p.fin = fin_cfg(*a.cfg);
     if (a.host_state)
@@ -784,8 +789,7 @@ int launch_staged(const PassArgs &a, cudaStream_t stream)
     p.stages = stages;
     p.n = L.padded_numel;
     const zero_adam_cfg &c = *a.cfg;
-    p.cfg = CfgDev{c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, c.max_grad_norm,
-                   c.adamw ? 1 : 0, c.bias_correction ? 1 : 0};
+    p.cfg = make_cfg_dev(c);
     p.state = a.state;
     p.w0 = p.wo0 = a.master[0];
     p.w1 = p.wo1 = a.master[1];
