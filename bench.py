@@ -571,6 +571,35 @@ def run_e2e(z, grads, wl, args, steps: int = 20):
             "h2d": "the step's kernels load the gradients from page-locked host memory"}
 
 
+def run_host_overhead(calls: int = 2000):
+    """--host-overhead: host time per zero_step_fused call (CPU timer around
+    `calls` enqueues, the device nearly idle: each step is small) for three
+    group shapes: 16 ranks every rank (131,072 parameters), one rank of 64
+    (262,144), 2 ranks (1,048,576).  Prints one JSON line."""
+    import torch
+    import zero_partitioned_mixed_step_gb300 as zs
+    torch.cuda.set_device(0)
+    out = {}
+    for world, n, rank in ((16, 16 * 8192, -1), (64, 64 * 4096, 0), (2, 1 << 20, -1)):
+        z = zs.ZeroStep((n,), world, zs.F16, zs.adam_cfg(), rank=rank)
+        grads = [torch.zeros(z.grad_numel(), dtype=torch.float16, device="cuda")
+                 for _ in range(world)]
+        for _ in range(20):
+            z.step(grads)
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(5):
+            t0 = time.perf_counter()
+            for _ in range(calls):
+                z.step(grads)
+            per.append((time.perf_counter() - t0) / calls * 1e6)
+            torch.cuda.synchronize()
+        out[f"world{world}_rank{rank}_n{n}"] = {"us_per_call_median": statistics.median(per),
+                                                 "us_per_call_min": min(per)}
+    print(json.dumps({"host_overhead": out, "calls": calls,
+                      "what": "ZeroStep.step -> zero_step_fused enqueue, ctypes included"}))
+
+
 def main():
     from synth.workloads import BY_NAME, CFG3
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
@@ -579,7 +608,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=CFG3.name, choices=sorted(BY_NAME))
+    ap.add_argument("--host-overhead", action="store_true",
+                    help="print the host time per step call instead of the benchmark")
     args = ap.parse_args()
+    if args.host_overhead:
+        run_host_overhead()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = BY_NAME[args.workload]
