@@ -81,8 +81,13 @@ def _grad_array(tensors: Sequence[torch.Tensor]):
 
 
 def _stream(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    """The raw CUDA stream handle: the given stream, else torch's current one."""
+    if stream is not None:
+        return stream.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:  # the handle itself, without building a Stream object
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 # ----------------------------------------------------------------- host helpers
@@ -406,10 +411,26 @@ class ZeroStep:
         """Elements of each rank's gradient buffer."""
         return self.layout.owned_numel if self.grads_are_slices else self.layout.padded_numel
 
+    def _slots(self):
+        """The ctypes arrays of the ping-pong slots, built once per set of
+        slot tensors (the tensors are owned by this object)."""
+        key = tuple(map(id, (*self.master, *self.m, *self.v, *self.params)))
+        if getattr(self, "_slots_key", None) != key:
+            self._slot_arrays = (_state_array(self.master), _state_array(self.m),
+                                 _state_array(self.v), _ptr_array(self.params))
+            self._slots_key = key
+        return self._slot_arrays
+
     def step(self, grads: Sequence[torch.Tensor], stream=None) -> None:
-        zero_step_fused(grads, self.layout, self.master, self.m, self.v, self.params, self.cfg,
-                        self.state, self.ws, self.rank, self.g_stage, self.grads_are_slices,
-                        stream, self.half_reduce)
+        """The whole step (zero_step_fused) on this group's buffers."""
+        w, m, v, p = self._slots()
+        ws = self.ws
+        check("zero_step_fused",
+              lib().zero_step_fused(_grad_array(grads), int(self.grads_are_slices),
+                                    _grad_code(grads, self.half_reduce), ctypes.byref(self.layout),
+                                    self.rank, w, m, v, p, _dev_ptr(self.g_stage),
+                                    ctypes.byref(self.cfg), _dev_ptr(self.state), _dev_ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)))
 
     def step_buckets(self, grads: Sequence[torch.Tensor], first_bucket: int, n_buckets: int,
                      stream=None) -> None:
