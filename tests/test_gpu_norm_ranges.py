@@ -96,8 +96,11 @@ def _ranges(nb):
         [(0, 1), (1, 1), (2, nb - 2)]
 
 
+@pytest.mark.parametrize("where", ["device", "host"], ids=["grads-on-device", "grads-in-host"])
 @pytest.mark.parametrize("name", list(RANGE_CASES))
-def test_clipped_bucket_ranges_equal_fused_step(name):
+def test_clipped_bucket_ranges_equal_fused_step(name, where):
+    """The ranges may also load the gradients straight from page-locked host
+    memory (the first pass, and the second pass when it reduces again)."""
     base, stage = RANGE_CASES[name]
     lay = oracle.layout(base.numels, base.world, base.align, base.bucket)
     nb = lay.num_buckets if base.bucket else 1
@@ -129,6 +132,8 @@ def test_clipped_bucket_ranges_equal_fused_step(name):
         grads = gen_grads(wl, ref.lay, s, ref.st.loss_scale)
         ref.step(grads)
         gd = [to_dev_half(g, wl.dtype) for g in grads]
+        if where == "host":
+            gd = [zs.host_empty(g.numel(), g.dtype).copy_(g.cpu()) for g in gd]
         fork()
         for i, (f, n) in enumerate(ranges):
             alt.z.pass1_buckets(gd, f, n, side[i % 2])
