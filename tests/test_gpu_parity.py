@@ -121,6 +121,12 @@ EDGE = {
     "rank-view-full-buffers": CFG4.replace(numels=(16 * 4096 + 100,), world=16, rank=7,
                                            grads_are_slices=False, steps=2),
     "clip-never-active": CFG2.replace(numels=(50_000,), world=2, max_grad_norm=1e6, steps=2),
+    # the norm's tree over the most ranks the ABI accepts (1024 rank sums added in order),
+    # and over 100 ranks in buckets whose superchunks span several buckets
+    "clip-world-1024": CFG2.replace(numels=(1024 * 512 + 8,), world=1024, steps=2,
+                                    max_grad_norm=0.05),
+    "clip-world-100-buckets": CFG2.replace(numels=(100 * 8 * 700 + 13, 999), world=100,
+                                           bucket=100 * 8 * 64, steps=2, max_grad_norm=0.05),
 }
 
 
