@@ -19,6 +19,7 @@ Prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -564,7 +565,7 @@ def run_e2e(z, grads, wl, args, steps: int = 20):
     del host
     med = statistics.median(times)
     return {"value": params / med / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": 64, "steps": steps, "stat": "median of per-step rates",
+            "d2h_bytes_per_step": ctypes.sizeof(zs.StepState), "steps": steps, "stat": "median of per-step rates",
             "min": params / max(times) / 1e9, "max": params / min(times) / 1e9,
             "link_gbs": h2d / med / 1e9, "link_gbs_min": h2d / max(times) / 1e9,
             "link_gbs_max": h2d / min(times) / 1e9,

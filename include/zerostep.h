@@ -156,11 +156,12 @@ typedef struct {
 } zero_adam_cfg;
 
 /*
- * Step state, DEVICE-resident (64 bytes, 8-byte aligned), owned by the
+ * Step state, DEVICE-resident (192 bytes, 8-byte aligned), owned by the
  * caller.  Initialise a host copy with zero_state_init and copy it to the
  * device.  The kernels read it at the start of a step and zero_step_finalize
  * (or the last kernel of zero_step_fused / zero_step_fused_accumulated)
- * updates it at the end.
+ * updates it at the end.  The first 64 bytes are the step's state proper;
+ * scalar_cache is the library's own (below).
  */
 typedef struct {
     int64_t t;          /* committed (not skipped) steps */
@@ -179,13 +180,25 @@ typedef struct {
     int32_t skipped;    /* number of skipped steps */
     int32_t error;      /* nonzero if a kernel gave up waiting for its own memory copies
                            (never expected; that step was skipped); 0 at init */
+    /* Library-internal: the bias-correction scalars of the next step
+       (lr / (1 - beta1^t) and sqrt(1 - beta2^t), each rounded to binary32),
+       formed by one thread of the step before, off the step's critical path,
+       so that a step's CTAs need no binary64 division or square root.  Two
+       entries, one per ping-pong slot; each records every input of its
+       values (lr, beta1, beta2, beta1_pow, beta2_pow) and is used only when
+       all of them are bit for bit the step's own, otherwise the step forms
+       the scalars itself: a changed learning rate or betas, a restored state
+       or a skipped step never see stale values.  zero_state_init zero-fills
+       it; keep it as the library left it (copying the whole struct is fine). */
+    uint64_t scalar_cache[16];
 } zero_step_state;
 
 /* Human-readable text for a return code (static storage). */
 ZERO_API const char *zero_strerror(int code);
 
-/* ABI version: 2 (zero_workspace_bytes takes the layout; the clipped step's
- * bucket-range passes). */
+/* ABI version: 3 (2: zero_workspace_bytes takes the layout, the clipped
+ * step's bucket-range passes; 3: zero_step_state carries the scalar cache and
+ * is 192 bytes). */
 ZERO_API int zero_version(void);
 
 /*

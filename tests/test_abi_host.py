@@ -200,6 +200,9 @@ def test_state_init_and_workspace(zs):
     s = zs.zero_state_init(4096.0)
     assert (s.t, s.beta1_pow, s.beta2_pow, s.loss_scale, s.clip_coef, s.cur, s.found_inf) == \
         (0, 1.0, 1.0, 4096.0, 1.0, 0, 0)
+    # the library's scalar cache follows the 64 bytes of the state proper, zero-filled
+    assert zs.StepState.scalar_cache.offset == 64 and ctypes.sizeof(zs.StepState) == 192
+    assert bytes(s)[64:] == bytes(128)
     lib = zs._abi.lib()
     st = zs.StepState()
     for bad in (0.0, -2.0, 3.0, float("inf"), float("nan")):

@@ -26,7 +26,8 @@ import torch
 import oracle
 import zero_partitioned_mixed_step_gb300 as zs
 from gpu_norm_cases import NORM_CASES, RANGE_CASES
-from zs_harness import INF_BITS, SUMSQ_RTOL, Lockstep, gen_grads, rank_index, to_dev_half
+from zs_harness import (INF_BITS, SUMSQ_RTOL, Lockstep, gen_grads, rank_index, state_proper,
+                        to_dev_half)
 
 pytestmark = pytest.mark.gpu
 
@@ -146,7 +147,7 @@ def test_clipped_bucket_ranges_equal_fused_step(name, where):
         alt.z.commit(s0)
         torch.cuda.synchronize()
         a, b = ref.z.read_state(), alt.z.read_state()
-        assert bytes(a) == bytes(b), s
+        assert state_proper(a) == state_proper(b), s
         assert b.overflow == (1 if s == 2 else 0) and b.error == 0
         for x, y in zip(ref.z.current(), alt.z.current()):
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), s
@@ -188,7 +189,7 @@ def test_one_step_workspace_serves_every_view():
             ls.step(grads)
         torch.cuda.synchronize()
         for a, b in ((shared_all, own_all), (shared_one, own_one)):
-            assert bytes(a.z.read_state()) == bytes(b.z.read_state()), s
+            assert state_proper(a.z.read_state()) == state_proper(b.z.read_state()), s
             for x, y in zip(a.z.current(), b.z.current()):
                 assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), s
     own_all.check()

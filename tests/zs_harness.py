@@ -36,6 +36,12 @@ def lib_cfg(wl, **kw):
     return zs.adam_cfg(**args)
 
 
+def state_proper(st: "zs.StepState") -> bytes:
+    """The step state's own fields (the 64 bytes before the library's scalar
+    cache, which depends on which kernels ran, not on the step's result)."""
+    return bytes(st)[:zs.StepState.scalar_cache.offset]
+
+
 def tensor_mask(lay: oracle.Layout) -> np.ndarray:
     mask = np.zeros(lay.padded, bool)
     for o, n in zip(lay.offsets, lay.numels):

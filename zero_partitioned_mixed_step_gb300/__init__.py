@@ -163,7 +163,7 @@ def adam_cfg(lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999, eps: fl
 
 
 def new_state(loss_scale: float = 1.0, device="cuda") -> torch.Tensor:
-    """A device-resident zero_step_state (64 bytes) in its initial state."""
+    """A device-resident zero_step_state (192 bytes) in its initial state."""
     s = zero_state_init(loss_scale)
     host = torch.frombuffer(bytearray(bytes(s)), dtype=torch.uint8)
     return host.to(device)
@@ -491,7 +491,7 @@ class ZeroStep:
         reduced into the fp32 accumulator before the step."""
         s = stream if stream is not None else torch.cuda.current_stream()
         if getattr(self, "_state_host", None) is None:
-            self._state_host = host_empty(64, torch.uint8)
+            self._state_host = host_empty(ctypes.sizeof(StepState), torch.uint8)
         with torch.cuda.stream(s):
             for k in range(micro_steps):
                 grads = host_grads

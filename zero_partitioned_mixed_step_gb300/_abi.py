@@ -41,10 +41,11 @@ class StepState(ctypes.Structure):
                 ("loss_scale", ctypes.c_float), ("clip_coef", ctypes.c_float),
                 ("good_steps", ctypes.c_int32), ("overflow", ctypes.c_int32),
                 ("found_inf", ctypes.c_int32), ("cur", ctypes.c_int32),
-                ("skipped", ctypes.c_int32), ("error", ctypes.c_int32)]
+                ("skipped", ctypes.c_int32), ("error", ctypes.c_int32),
+                ("scalar_cache", ctypes.c_uint64 * 16)]
 
 
-assert ctypes.sizeof(StepState) == 64
+assert ctypes.sizeof(StepState) == 192
 assert ctypes.sizeof(Layout) == 72
 
 # Every symbol include/zerostep.h declares, with its ctypes signature.

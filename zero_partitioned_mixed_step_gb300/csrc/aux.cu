@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads)
 {
     __shared__ Scalars sh;
     __shared__ int sh_cur;
-    form_scalars(cfg, st, &st->sumsq, sh, sh_cur);
+    form_scalars<true>(cfg, st, &st->sumsq, sh, sh_cur);
     __syncthreads();
     const Scalars s = sh;
     if (s.skip)

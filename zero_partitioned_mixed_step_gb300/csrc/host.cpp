@@ -140,7 +140,7 @@ const char *zero_strerror(int code)
     }
 }
 
-int zero_version(void) { return 2; }
+int zero_version(void) { return 3; }
 
 int zero_partition_layout(int n_tensors, const int64_t *numel, int world, int align_elems,
                           int64_t bucket_numel, int64_t *tensor_offset_out, zero_layout *out)

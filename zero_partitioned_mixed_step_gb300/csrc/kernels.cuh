@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "internal.h"
@@ -377,18 +378,55 @@ __device__ __forceinline__ float clip_coefficient(double sumsq, double max_norm)
     return __double2float_rn(fmin(1.0, __ddiv_rn(max_norm, __dadd_rn(__dsqrt_rn(sumsq), 1e-6))));
 }
 
-// Scalars of step t + 1 from the state at the start of the step, formed by
-// three threads of different warps so that the binary64 division and square
-// roots (slow on GB300's binary64 pipe) run at the same time on different
-// sub-partitions: thread 0 reads the state's flags and forms step = lr /
-// (1 - beta1^t) (beta1^t = beta1_pow * beta1), thread 32 forms rbc2 =
-// sqrt(1 - beta2^t), thread 64 the clip coefficient when `total` (the step's
-// global sum of squares) is given.  The configuration-only values were rounded
-// on the host (make_cfg_dev).  A barrier must follow before sh is read; every
-// CTA has at least 96 threads.
+// One entry of zero_step_state::scalar_cache: the bias-correction scalars of
+// one step and every input they were formed from.
+struct ScalarCacheEntry {
+    double lr, beta1, beta2;
+    double beta1_pow, beta2_pow;  // the state's beta powers at the start of that step
+    float step, rbc2;
+    uint32_t tag, pad0;
+    uint64_t pad1;
+};
+static_assert(sizeof(ScalarCacheEntry) == 64, "two entries fill scalar_cache");
+static_assert(offsetof(zero_step_state, scalar_cache) == 64 && sizeof(zero_step_state) == 192,
+              "zero_step_state layout");
+constexpr uint32_t kScalarCacheTag = 0x5a530c01u;  // marks an entry the library wrote
+
+__device__ __forceinline__ bool same_bits(double a, double b)
+{
+    return __double_as_longlong(a) == __double_as_longlong(b);
+}
+
+// step = lr / (1 - beta1^t) and rbc2 = sqrt(1 - beta2^t) from the beta powers
+// at the start of the step (beta^t = beta_pow * beta), in binary64 rounded
+// once to binary32.
+__device__ __forceinline__ float bias_step(const CfgDev &c, double beta1_pow)
+{
+    return __double2float_rn(__ddiv_rn(c.lr, __dsub_rn(1.0, __dmul_rn(beta1_pow, c.beta1))));
+}
+
+__device__ __forceinline__ float bias_rbc2(const CfgDev &c, double beta2_pow)
+{
+    return __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, __dmul_rn(beta2_pow, c.beta2))));
+}
+
+// Scalars of step t + 1 from the state at the start of the step.  Thread 0
+// reads the state's flags and the slot; step and rbc2 come from the scalar
+// cache entry of the slot when that entry was formed from exactly this
+// step's lr, betas and beta powers (the values are then the ones the formula
+// gives), else thread 0 forms step and thread 32 rbc2 here, in different
+// warps so that the binary64 division and square root (slow on GB300's
+// binary64 pipe) overlap.  Each of the two threads loads both entries along
+// with the state, so that no load waits on the slot index.  Thread 64 forms
+// the clip coefficient when `total` (the step's global sum of squares) is
+// given.  ADAM = false (a first pass) forms only the flags, the slot and
+// 1/S.  The configuration-only values were rounded on the host (make_cfg_dev).
+// A barrier must follow before sh is read; every CTA has at least 96 threads.
+template <bool ADAM>
 __device__ __forceinline__ void form_scalars(const CfgDev &c, const zero_step_state *st,
                                              const double *total, Scalars &sh, int &sh_cur)
 {
+    const ScalarCacheEntry *e = reinterpret_cast<const ScalarCacheEntry *>(st->scalar_cache);
     if (threadIdx.x == 0) {
         sh.b1 = c.b1;
         sh.omb1 = c.omb1;
@@ -401,19 +439,87 @@ __device__ __forceinline__ void form_scalars(const CfgDev &c, const zero_step_st
         sh.clip = c.max_norm > 0.0;
         sh.inv_s = __fdiv_rn(1.0f, st->loss_scale);
         sh.skip = st->found_inf & 1;
-        sh_cur = st->cur;
-        sh.step = c.bias_correction
-                      ? __double2float_rn(__ddiv_rn(c.lr, __dsub_rn(1.0, __dmul_rn(st->beta1_pow,
-                                                                                   c.beta1))))
-                      : c.lr_f;
+        const int cur = st->cur;
+        sh_cur = cur;
+        if (ADAM) {
+            if (!c.bias_correction) {
+                sh.step = c.lr_f;
+            } else {
+                const double p = st->beta1_pow;
+                const uint32_t t0 = e[0].tag, t1 = e[1].tag;
+                const double l0 = e[0].lr, l1 = e[1].lr;
+                const double b0 = e[0].beta1, b1 = e[1].beta1;
+                const double q0 = e[0].beta1_pow, q1 = e[1].beta1_pow;
+                const float s0 = e[0].step, s1 = e[1].step;
+                const bool hit = cur ? t1 == kScalarCacheTag && same_bits(l1, c.lr) &&
+                                           same_bits(b1, c.beta1) && same_bits(q1, p)
+                                     : t0 == kScalarCacheTag && same_bits(l0, c.lr) &&
+                                           same_bits(b0, c.beta1) && same_bits(q0, p);
+                if (hit)
+                    sh.step = cur ? s1 : s0;
+                else
+                    sh.step = bias_step(c, p);
+            }
+        }
     } else if (threadIdx.x == 32) {
-        sh.rbc2 = c.bias_correction
-                      ? __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, __dmul_rn(st->beta2_pow,
-                                                                              c.beta2))))
-                      : 1.0f;
+        if (ADAM) {
+            if (!c.bias_correction) {
+                sh.rbc2 = 1.0f;
+            } else {
+                const int cur = st->cur;
+                const double p = st->beta2_pow;
+                const uint32_t t0 = e[0].tag, t1 = e[1].tag;
+                const double b0 = e[0].beta2, b1 = e[1].beta2;
+                const double q0 = e[0].beta2_pow, q1 = e[1].beta2_pow;
+                const float r0 = e[0].rbc2, r1 = e[1].rbc2;
+                const bool hit = cur ? t1 == kScalarCacheTag && same_bits(b1, c.beta2) &&
+                                           same_bits(q1, p)
+                                     : t0 == kScalarCacheTag && same_bits(b0, c.beta2) &&
+                                           same_bits(q0, p);
+                if (hit)
+                    sh.rbc2 = cur ? r1 : r0;
+                else
+                    sh.rbc2 = bias_rbc2(c, p);
+            }
+        }
     } else if (threadIdx.x == 64) {
         sh.coef = total && c.max_norm > 0.0 ? clip_coefficient(__ldcg(total), c.max_norm) : 1.0f;
     }
+}
+
+// One thread of a kernel that updates with the state read at its start, before
+// the kernel counts itself in found_inf (so before anything can end the
+// step): forms the scalars of the NEXT step as they will be if this step
+// commits (beta powers advanced by one factor, same configuration) into the
+// cache entry of slot 1 - cur, the slot the next step reads after a commit,
+// unless that entry holds them already.  If this step is skipped, the next
+// step reads slot cur again, whose entry still matches its unchanged beta
+// powers.  No reader uses entry 1 - cur while this step runs, and several
+// launches of one step (bucket ranges) write the same values.  The slot and
+// the beta powers are read here, not kept from the prologue, so that nothing
+// stays live across the kernel's main loop for it.
+__device__ __forceinline__ void form_next_scalars(const CfgDev &c, zero_step_state *st)
+{
+    if (!c.bias_correction)
+        return;
+    const int cur = st->cur;
+    const double p1 = __dmul_rn(st->beta1_pow, c.beta1);
+    const double p2 = __dmul_rn(st->beta2_pow, c.beta2);
+    ScalarCacheEntry *e = reinterpret_cast<ScalarCacheEntry *>(st->scalar_cache) + (cur ^ 1);
+    if (e->tag == kScalarCacheTag && same_bits(e->lr, c.lr) && same_bits(e->beta1, c.beta1) &&
+        same_bits(e->beta2, c.beta2) && same_bits(e->beta1_pow, p1) &&
+        same_bits(e->beta2_pow, p2))
+        return;
+    const float step = bias_step(c, p1);
+    const float rbc2 = bias_rbc2(c, p2);
+    e->lr = c.lr;
+    e->beta1 = c.beta1;
+    e->beta2 = c.beta2;
+    e->beta1_pow = p1;
+    e->beta2_pow = p2;
+    e->step = step;
+    e->rbc2 = rbc2;
+    e->tag = kScalarCacheTag;
 }
 
 // ------------------------------------------------------------------ end of step

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
     constexpr int gbytes = W * kStagedTile * 2;
     const int nst = p.stages;
     const int64_t tiles = (p.n + kStagedTile - 1) / kStagedTile;
-    form_scalars(p.cfg, p.state, nullptr, sh, sh_cur);
+    form_scalars<true>(p.cfg, p.state, nullptr, sh, sh_cur);
     if (tid == 0) {
         abort_flag = 0;
         for (int st = 0; st < nst; ++st) {
@@ -237,6 +237,9 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
             }
         }
     }
+    // the next step's bias-correction scalars, by the last CTA (the least work)
+    if (blockIdx.x == gridDim.x - 1 && tid == 0)
+        form_next_scalars(p.cfg, p.state);
     finish_cta(abort_flag || bad, p.end_step != 0, p.fin, p.state);
 }
 

@@ -121,6 +121,20 @@ __device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, Su
     });
 }
 
+// Instances with a lead CTA (step_body): the one-pass steps over at most 4
+// ranks, the small steps, where the prologue's binary64 division and square
+// root are a visible share of the step (1M elements over 2 ranks: 13.9 ->
+// 12.3 us, median of 300 steps with L2 flushed).  A larger step forms them in
+// its prologue (microseconds against milliseconds).  The branch is compiled
+// into these instances only: in the others it changed ptxas' register
+// allocation (the 64-rank shard's instance went from 80 to 64 registers and
+// from 2.57 to 2.62 ms per step; a writer at the end of a grid-stride CTA took
+// another from 80 to 112).
+__host__ __device__ constexpr bool has_lead(int dt, int w, int mode, bool host_state)
+{
+    return mode == M_FUSED && !host_state && w > 0 && w <= 4 && !half_reduce(dt);
+}
+
 // The body of the streaming kernels (the __global__ wrappers below differ
 // only in their launch bounds).
 template <int DT, int W, int MAXW, int MODE, bool ALL, bool HOST_STATE>
@@ -131,7 +145,23 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     Scalars s{};
     int cur = 0;
     const View &vw = p.view;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    // A one-pass step over at most 4 ranks whose units fit in one wave forms
+    // the next step's bias-correction scalars (form_next_scalars) in a CTA
+    // of its own, off the step's critical path: launch_one adds a CTA to the
+    // grid, and that CTA 0 ("lead") does only this, alongside the work CTAs
+    // 1, 2, ...  The grid tells: more CTAs than units / 256.  (See has_lead.)
+    constexpr bool kLead = has_lead(DT, W, MODE, HOST_STATE);
+    const int lead = kLead && (int64_t)gridDim.x > (vw.units + kThreads - 1) / kThreads ? 1 : 0;
+    if constexpr (kLead) {
+        if (lead && blockIdx.x == 0) {
+            if (threadIdx.x == 0)
+                form_next_scalars(p.cfg, p.state);
+            finish_cta(false, ends_step(MODE) && p.end_step, p.fin, p.state);
+            return;
+        }
+    }
+    const int64_t cta = (int64_t)blockIdx.x - lead;  // among the work CTAs
+    const int64_t stride = ((int64_t)gridDim.x - lead) * kThreads;
     const uint64_t pol = evict_first_policy();
     // One-pass steps over at most 4 ranks issue their first unit's loads
     // before the prologue's barrier (the gradients need nothing, the state
@@ -141,7 +171,7 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     // fewer; at 2 ranks it went from 78 to 64, a CTA per SM more.)
     constexpr bool kEarly = MODE == M_FUSED && !HOST_STATE && W > 0 && W <= 4 &&
                             !half_reduce(DT);
-    const int64_t u_first = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t u_first = cta * kThreads + threadIdx.x;
     uint4 early_g[kEarly ? W : 1];
     float early_w[8], early_m[8], early_v[8];
     int64_t early_f = 0, early_si = 0;
@@ -162,12 +192,14 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
         // A second pass also forms the clip coefficient from the global sum
         // of squares the first pass formed; CTA 0 publishes both in the state
         // when the step is not skipped.
-        form_scalars(p.cfg, p.state, second_pass(MODE) ? p.norm_total : nullptr, sh, sh_cur);
+        form_scalars<!sums_squares(MODE)>(p.cfg, p.state,
+                                          second_pass(MODE) ? p.norm_total : nullptr, sh,
+                                          sh_cur);
         __syncthreads();
         s = sh;
         cur = sh_cur;
         if constexpr (second_pass(MODE)) {
-            if (blockIdx.x == 0 && threadIdx.x == 0 && !s.skip) {
+            if (cta == 0 && threadIdx.x == 0 && !s.skip) {
                 p.state->sumsq = __ldcg(p.norm_total);
                 p.state->clip_coef = s.coef;
             }
@@ -179,8 +211,7 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
             work = false;
             if constexpr (MODE == M_PASS2_STAGED) {
                 if (p.discard)  // the kept stage lines are not needed either
-                    for (int64_t u = p.keep_from +
-                                     4 * ((int64_t)blockIdx.x * kThreads + threadIdx.x);
+                    for (int64_t u = p.keep_from + 4 * (cta * kThreads + threadIdx.x);
                          u + 4 <= vw.units; u += 4 * stride)
                         discard_l2_line(p.stage + u * kUnit);
             }
@@ -288,7 +319,7 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
         st_half8(out + f, pack_half8<DT>(w), pol);
     };
 
-    const int64_t base = (int64_t)blockIdx.x * kThreads;
+    const int64_t base = cta * kThreads;
     if constexpr (sums_squares(MODE)) {
         norm_loop<ALL>(p.norm, vw, ss, unit);
     } else if constexpr (second_pass(MODE)) {
@@ -397,7 +428,12 @@ int launch_one(const StepParams<MAXW> &p, cudaStream_t stream, int *gx_out)
         target = device_sms() * kHostAllCtasPerSm;
     const int64_t want = sums_squares(MODE) ? p.norm.launch_chunks
                                             : (p.view.units + kThreads - 1) / kThreads;
-    const int64_t gx = want < 1 ? 1 : (want < target ? want : target);
+    int64_t gx = want < 1 ? 1 : (want < target ? want : target);
+    // A small one-pass step whose units fit in one wave with a CTA to spare
+    // gets a lead CTA that forms the next step's bias-correction scalars
+    // (step_body tells it from the grid: more CTAs than units / 256).
+    if (has_lead(DT, W, MODE, HOST_STATE) && p.cfg.bias_correction && want + 1 <= target)
+        gx = want + 1;
     if (gx_out)
         *gx_out = (int)gx;
     kern<<<(unsigned)gx, kThreads, 0, stream>>>(p);
