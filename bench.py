@@ -468,6 +468,33 @@ def run_ours(args, wl):
     total_ms = max_over_ranks(region_ms)
     st = z.read_state()
 
+    # A step that fits in L2 cannot reach the copy bandwidth of a large copy:
+    # time torch's device copy of the same bytes (half read, half written)
+    # the same way (L2 flushed before each, per-copy events) for context.
+    size_copy = None
+    if flush is not None:
+        half = max(1, n_elems * bpe // 2 // 4)
+        src = torch.ones(half, dtype=torch.float32, device=device)
+        dst = torch.empty_like(src)
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nsteps)]
+        for k in range(-3, nsteps):
+            flush.fill_(float(k))
+            if k >= 0:
+                cev[k][0].record(stream)
+            dst.copy_(src)
+            if k >= 0:
+                cev[k][1].record(stream)
+        torch.cuda.synchronize()
+        copy_ms = statistics.median(a.elapsed_time(b) for a, b in cev)
+        size_copy = {"bytes": 2 * half * 4, "median_ms": copy_ms,
+                     "step_median_ms": statistics.median(step_ms),
+                     "gbs": 2 * half * 4 / (copy_ms / 1e3) / 1e9,
+                     "note": "torch's device copy of the step's bytes (half read, half "
+                             "written), L2 flushed before each like the steps: what a copy "
+                             "reaches at this size"}
+        del src, dst
+
     # end to end: the same step through the public API from pinned host buffers
     e2e = run_e2e(z, grads, wl, args)
 
@@ -524,6 +551,7 @@ def run_ours(args, wl):
                           "note": "master/m/v read and written in Grace memory over NVLink-C2C"}}
            if wl.offload_state else {}),
         **pipeline,
+        **({"size_matched_copy": size_copy} if size_copy else {}),
         "clocks": clocks.summary(),
     }
     print(json.dumps(line))
