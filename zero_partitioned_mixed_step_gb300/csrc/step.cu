@@ -190,8 +190,8 @@ __device__ __forceinline__ void step_body(const StepParams<MAXW> &p)
     }
     if constexpr (!reduces_only(MODE)) {
         // A second pass also forms the clip coefficient from the global sum
-        // of squares the first pass formed; CTA 0 publishes both in the state
-        // when the step is not skipped.
+        // of squares the first pass formed; the first work CTA publishes both
+        // in the state when the step is not skipped.
         form_scalars<!sums_squares(MODE)>(p.cfg, p.state,
                                           second_pass(MODE) ? p.norm_total : nullptr, sh,
                                           sh_cur);
