@@ -75,6 +75,37 @@ def norm_bits():
     return out
 
 
+def small_steps():
+    """One-pass steps over 2 and 4 ranks (the instances that get a lead CTA
+    when their units fit in one wave), four steps each with the learning rate
+    changed every step and an Inf in step 2: digests of every buffer and of
+    the 64 bytes of state proper, and whether the scalar cache was written."""
+    import torch
+    from synth.workloads import BF16, CFG1
+    from zs_harness import Lockstep, gen_grads, state_proper, to_dev_half
+    cases = {
+        "nd2-fp16": CFG1.replace(numels=(300_001,), steps=4, inject_at=((2, 0, 150_000),)),
+        "nd4-bf16": CFG1.replace(numels=(200_003, 77), world=4, dtype=BF16, steps=4,
+                                 inject_at=((2, 3, 100_000),)),
+    }
+    out = {"cap": os.environ.get("ZERO_TEST_MAX_CTAS")}
+    for name, wl in cases.items():
+        ls = Lockstep(wl)
+        for s, lr in zip(range(1, wl.steps + 1), (2e-4, 6e-4, 1e-3, 5e-4)):
+            ls.ocfg.lr = lr
+            ls.z.cfg.lr = lr
+            ls.step(gen_grads(wl, ls.lay, s, ls.st.loss_scale))
+            ls.check()
+        h = hashlib.sha256()
+        for t in ls.z.current():
+            h.update(t.detach().cpu().contiguous().view(torch.uint8).numpy().tobytes())
+        st = ls.z.read_state()
+        h.update(state_proper(st))
+        out[name] = {"digest": h.hexdigest(), "cache_written": any(st.scalar_cache)}
+    return out
+
+
 if __name__ == "__main__":
-    result = {"staged_wait": staged_wait, "norm_bits": norm_bits}[sys.argv[1]]()
+    result = {"staged_wait": staged_wait, "norm_bits": norm_bits,
+              "small_steps": small_steps}[sys.argv[1]]()
     print(json.dumps(result))

@@ -10,7 +10,11 @@ formula.
     skipped step and caches zeroed, swapped or left over from an earlier
     step all give the oracle's results and the same bits as an untouched
     run (a key that does not match makes the step form its scalars)."""
+import json
+import os
 import struct
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -121,3 +125,27 @@ def test_schedules_and_rewritten_caches_match_the_oracle(name):
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), s
     assert keep.st.skipped == 1 and keep.st.t == wl.steps - 1
 
+
+
+def _child(name, **env):
+    e = dict(os.environ)
+    e.pop("ZERO_TEST_MAX_CTAS", None)
+    e.update(env)
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "gpu_children.py"), name],
+                       capture_output=True, text=True, env=e, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def test_small_steps_give_the_same_bits_with_and_without_a_lead_cta():
+    """The small one-pass steps with their lead CTA (every unit in one wave,
+    the next step's scalars formed alongside) and the same steps with every
+    grid capped at 7 CTAs (grid-stride, no lead CTA, scalars formed in every
+    CTA's prologue) follow the oracle and give the same buffers and state."""
+    lead = _child("small_steps")
+    capped = _child("small_steps", ZERO_TEST_MAX_CTAS="7")
+    assert lead.pop("cap") is None and capped.pop("cap") == "7"
+    for name in lead:
+        assert lead[name]["digest"] == capped[name]["digest"], name
+        assert lead[name]["cache_written"] and not capped[name]["cache_written"], name
