@@ -42,6 +42,13 @@ def test_exports_every_declared_symbol(zs):
     assert set(names) == set(zs._abi.SIGNATURES)
 
 
+def test_abi_version_matches_header(zs):
+    """zero_version() is the version the header states (3: the step state
+    carries the scalar cache and is 192 bytes)."""
+    m = re.search(r"ABI version: (\d+)", open(HEADER).read())
+    assert m and zs._abi.lib().zero_version() == int(m.group(1)) == 3
+
+
 def test_exports_nothing_else(zs):
     """Only the declared entry points are dynamic symbols of the library
     (it is built with hidden visibility), so internal state such as cached
