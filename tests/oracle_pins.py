@@ -279,6 +279,42 @@ def pin_adam_literal_form():
     assert np.all(np.abs(w - want) <= 8 * U32 * (np.abs(want) + 1e-3))
 
 
+def _ulp32(x: Fraction) -> Fraction:
+    """The binary32 spacing at positive x (normal range)."""
+    _, e = math.frexp(float(x))
+    return Fraction(2) ** (e - 24)
+
+
+def pin_step_scalars():
+    """The per-step scalars of step t (after t - 1 committed steps) against
+    exact rational arithmetic: step = lr / (1 - beta1^t) and
+    rbc2 = sqrt(1 - beta2^t), each within one binary32 ulp of the exact value
+    (the running binary64 products of the betas stay within about t 2^-53 of
+    beta^t, far inside half a binary32 ulp), over 60 committed steps; a
+    skipped step changes neither; without bias correction step = lr and
+    rbc2 = 1.  ("DeepSpeed ZeRO", 以 AdaW 为例, with the bias correction the
+    textbook update adds.)"""
+    for lr, b1, b2 in ((1e-3, 0.9, 0.999), (3e-4, 0.85, 0.995), (2.0 ** -10, 0.5, 0.75)):
+        cfg = oracle.AdamCfg(lr=lr, beta1=b1, beta2=b2)
+        st = oracle.State()
+        for t in range(1, 61):
+            sc = oracle.step_scalars(cfg, st)
+            want = Fraction(lr) / (1 - Fraction(b1) ** t)
+            assert abs(Fraction(sc.step) - want) <= _ulp32(want), (lr, t, sc.step)
+            y = 1 - Fraction(b2) ** t
+            r, u = Fraction(sc.rbc2), _ulp32(Fraction(sc.rbc2))
+            assert (r - u) ** 2 <= y <= (r + u) ** 2, (b2, t, sc.rbc2)
+            if t % 7 == 0:  # an overflow step in between changes nothing
+                oracle.skip(cfg, st)
+                assert bytes(oracle.step_scalars(cfg, st)) == bytes(sc)
+            oracle.commit(cfg, st)
+        assert st.t == 60
+    cfg = oracle.AdamCfg(lr=1e-3, bias_correction=False)
+    st = oracle.State(t=5, bp1=0.9 ** 5, bp2=0.999 ** 5)
+    sc = oracle.step_scalars(cfg, st)
+    assert sc.step == np.float32(1e-3) and sc.rbc2 == 1.0
+
+
 def _torch_reference(g_list, w0, cfg, cls):
     p = torch.nn.Parameter(torch.from_numpy(w0.astype(np.float64)))
     opt = cls([p], lr=cfg.lr, betas=(cfg.beta1, cfg.beta2), eps=cfg.eps,
@@ -757,4 +793,4 @@ ALL_PINS = [pin_memory_closed_forms, pin_decode_exhaustive, pin_encode_structure
             pin_adam_literal_form, pin_vs_torch, pin_partition_concat, pin_skip_invariance,
             pin_loss_scale_growth, pin_clip, pin_layout, pin_accumulate_exact,
             pin_accumulate_order, pin_accumulated_step, pin_half_reduce,
-            pin_windowed_matches_step]
+            pin_windowed_matches_step, pin_step_scalars]
