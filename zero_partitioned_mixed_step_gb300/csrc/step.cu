@@ -123,9 +123,10 @@ __device__ __forceinline__ void norm_loop(const NormPlan &np, const View &vw, Su
 
 // Instances with a lead CTA (step_body): the one-pass steps over at most 4
 // ranks, the small steps, where the prologue's binary64 division and square
-// root are a visible share of the step (1M elements over 2 ranks: 13.9 ->
-// 12.3 us, median of 300 steps with L2 flushed).  A larger step forms them in
-// its prologue (microseconds against milliseconds).  The branch is compiled
+// root are a visible share of the step (1M elements over 2 ranks, median of
+// 300 steps with L2 flushed: 13.9 -> 12.3 us on one GB300, 12.4-12.6 -> 12.3
+// us on another).  A larger step forms them in its prologue (microseconds
+// against milliseconds).  The branch is compiled
 // into these instances only: in the others it changed ptxas' register
 // allocation (the 64-rank shard's instance went from 80 to 64 registers and
 // from 2.57 to 2.62 ms per step; a writer at the end of a grid-stride CTA took
