@@ -183,13 +183,16 @@ typedef struct {
     /* Library-internal: the bias-correction scalars of the next step
        (lr / (1 - beta1^t) and sqrt(1 - beta2^t), each rounded to binary32),
        formed by one thread of the step before, off the step's critical path,
-       so that a step's CTAs need no binary64 division or square root.  Two
-       entries, one per ping-pong slot; each records every input of its
-       values (lr, beta1, beta2, beta1_pow, beta2_pow) and is used only when
-       all of them are bit for bit the step's own, otherwise the step forms
-       the scalars itself: a changed learning rate or betas, a restored state
-       or a skipped step never see stale values.  zero_state_init zero-fills
-       it; keep it as the library left it (copying the whole struct is fine). */
+       so that the next step's CTAs need no binary64 division or square root.
+       The one-pass kernels of small steps over at most 4 ranks and the
+       N_d = 16 staged kernel form them; other kernels leave the cache as it
+       is.  Two entries, one per ping-pong slot; each records every input of
+       its values (lr, beta1, beta2, beta1_pow, beta2_pow) and is used only
+       when all of them are bit for bit the step's own, otherwise the step
+       forms the scalars itself: a changed learning rate or betas, a restored
+       state or a skipped step never see stale values.  zero_state_init
+       zero-fills it; keep it as the library left it (copying the whole
+       struct is fine). */
     uint64_t scalar_cache[16];
 } zero_step_state;
 
